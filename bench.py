@@ -1,0 +1,371 @@
+"""Benchmark of one DDTree verify step on GB300.
+
+A step is the whole hot path on one batch: ddt_build_tree ->
+ddt_compile_visibility -> ddt_verify_attn (split-KV partial + combine) ->
+ddt_accept, captured once in a CUDA graph and replayed.  Inputs are seeded
+and synthetic (workload "single_p4096_b32_h64": 1 request, prefix 4096,
+budget 32, 64 heads, 576-wide bf16 latent rows in a 65536-row pool) and
+resident in HBM; L2 is flushed (a 256 MiB write) before every timed step.
+
+The reported metric is verify-attention TFLOP/s: algorithmic attention FLOPs
+(2 * (576 + 512) per visible (query-head, kv) pair) per second of the whole
+step.  KV GB/s, steps/s, a roofline object for ddt_verify_attn (timed with
+CUDA events inside the same region), an end-to-end figure through host
+buffers, and the CPU oracle timed on the host cores are printed beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+For N > 1 (torchrun) every rank runs its own copy of the workload (weak
+scaling, no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "single_p4096_b32_h64"
+METRIC = "verify-attn TFLOP/s and KV GB/s per step, % of roofline, 1xGB300"
+PROFILE_TRAFFIC = None  # dram bytes per ddt_verify_attn call from ncu; null until captured
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# -- timing aggregation shared by all ranks (tested on CPU with gloo) -----------
+def reduce_over_ranks(elapsed_s: float, units: float, dist=None):
+    """Max of the per-rank elapsed time and sum of per-rank units (FLOPs)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return elapsed_s, units
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except Exception:
+            pass
+        if self.path:
+            os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_device(args, rank, world, local_rank):
+    import torch
+
+    from tree_speculative_decoding_gb300 import workloads
+    from tree_speculative_decoding_gb300.metrics import attn_flops, kv_bytes
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    wl = workloads.preset(args.workload)
+    st = VerifyStep(wl, dev)
+    st.run()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    depth = st.depth.cpu().numpy()
+    flops = attn_flops(wl.prefix_len, depth, wl.qo_indptr, wl.H)
+    kvb = kv_bytes(wl.kv_indptr)
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            st.run(stream=stream)
+    torch.cuda.synchronize()
+
+    # kernels launched per step: tree, mask, attention partial (+ combine), accept
+    launches_per_step = 4 + (1 if st.num_splits > 1 else 0)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def one_step(ev):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            ev[0].record(stream)
+            graph.replay()
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step([torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)])
+    torch.cuda.synchronize()
+
+    # separate, identically flushed loop timing ddt_verify_attn alone (its own
+    # events on the same stream) for the roofline object
+    attn_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(attn_graph, stream=stream):
+            st.verify_attn(stream=stream)
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+              for _ in range(args.steps)]
+    attn_events = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                   for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            one_step(events[i])
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                attn_events[i][0].record(stream)
+                attn_graph.replay()
+                attn_events[i][1].record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = clk.summary()
+    step_ms = [a.elapsed_time(b) for a, b in events]
+    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    elapsed = sum(step_ms) / 1e3
+    elapsed_max, flops_all = reduce_over_ranks(elapsed, flops * args.steps, dist)
+
+    # end to end through host buffers: per-step inputs from pinned memory, the
+    # same graph, then the results back to pinned memory
+    h_in = {name: getattr(st, name).detach().cpu().pin_memory()
+            for name in ("topk_logp", "topk_ids", "root_id", "kv_indices", "q", "target_argmax")}
+    h_out = {name: torch.empty_like(getattr(st, name), device="cpu").pin_memory()
+             for name in ("out", "lse", "accept_len", "commit_tokens", "bonus")}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_steps = max(10, args.steps // 10)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+              for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e2e_ev[i][0].record(stream)
+            for name, t in h_in.items():
+                getattr(st, name).copy_(t, non_blocking=True)
+            graph.replay()
+            for name, t in h_out.items():
+                t.copy_(getattr(st, name), non_blocking=True)
+            e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    st.check_device_errors()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
+    ms_per_step = elapsed_max * 1e3 / args.steps
+    value = flops_all / elapsed_max / 1e12
+    attn_mean_ms = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean_ms / 1e3) / 1e12
+    t_roof_ms = max(flops / (tf_burst * 1e12), kvb / (hbm * 1e9)) * 1e3
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; N(0,1) bf16 q and latent KV; drafter top-k from "
+                "log-softmax of N(0,3) logits)",
+        "config": {"workload": WORKLOAD, "batch": wl.B, "heads": wl.H, "prefix": int(wl.prefix_len[0]),
+                   "budget": int(wl.budget[0]), "q_len": int(wl.q_len[0]), "topk": wl.K,
+                   "pool_rows": wl.pool_rows, "num_splits": st.num_splits,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "timing": "CUDA graph replay of the 4-stage step, CUDA events per step",
+                   "parallelism": f"replicas x{world}"},
+        "kv_gbs": round(kvb * args.steps * world / elapsed_max / 1e9, 2),
+        "steps_per_s": round(args.steps * world / elapsed_max, 1),
+        "attn_flops_per_step": flops,
+        "kv_bytes_per_step": kvb,
+        "verify_attn_ms": round(attn_mean_ms, 5),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4),
+                     "traffic": PROFILE_TRAFFIC, "peak_source": f"{peak_kind} bf16 burst",
+                     "kernel": "ddt_verify_attn (partial + combine)",
+                     "t_roof_ms": round(t_roof_ms, 5),
+                     "frac_of_sustained": round(achieved / tf_sus, 4)},
+        "e2e": {"value": round(flops / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def oracle_step(wl, rows=None):
+    """One verify step of the CPU oracle; returns attention FLOPs of the rows it computed."""
+    import oracle
+    from tree_speculative_decoding_gb300.metrics import attn_flops
+    tok, par, dep = oracle.build_tree(wl.topk_logp, wl.topk_ids, wl.root_id, wl.budget,
+                                      wl.qo_indptr, wl.max_depth, wl.K)
+    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    oracle.verify_attn(wl.q, wl.kv_pool, wl.kv_indices, wl.kv_indptr, wl.qo_indptr, mask, mip,
+                       wl.H, wl.scale, rows=rows)
+    oracle.accept(tok, par, wl.qo_indptr, wl.argmax_random, wl.max_depth)
+    full = attn_flops(wl.prefix_len, dep, wl.qo_indptr, wl.H)
+    if rows is None:
+        return full
+    return full * len(rows) / (wl.total_q * wl.H)
+
+
+def cpu_baseline(wl, seconds=10.0):
+    import oracle
+    oracle.build()
+    total, t0, reps = 0.0, time.perf_counter(), 0
+    while True:
+        total += oracle_step(wl)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full oracle verify steps of {WORKLOAD} (tree, mask, fp64 attention "
+                      f"over all {wl.total_q * wl.H} rows, accept) in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, on this workload."""
+    if rank != 0:
+        return None
+    import oracle
+    from tree_speculative_decoding_gb300 import workloads
+    oracle.build()
+    wl = workloads.preset(args.workload)
+    H = wl.H
+    # bounded sample per step: the first 256 rows (4 nodes x 64 heads) of the step
+    rows = np.arange(min(256, wl.total_q * H), dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_step(wl, rows)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_step(wl, rows)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"per step: oracle tree + mask + accept and fp64 attention for {len(rows)} of "
+              f"{wl.total_q * H} rows of {args.workload}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                             "cores": oracle.num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_device(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * ddt.h -- C ABI of the GB300 (sm_103a) DDTree verify step.
+ *
+ * Four stages of one speculative-decoding verify step, as defined on the pages
+ * "The DDTree CUDA Graph Fix: Unlocking Speculative Decoding at 109 tok/s on
+ * PCIe Blackwell" (section "The DDTree Architecture: Confirming Multiple-Path
+ * Evaluation"), "The Architecture of a Speculative Decoding Engine" (sections
+ * "The Final Resolution: A Concrete Trace" and "The Forward Pass Pseudocode")
+ * and "The 30-Column Mask" (sections "The Message: Tensor Shapes as Evidence",
+ * "The Fix: Building Combined Indices", "Mask Stride Formula"):
+ *
+ *   ddt_build_tree          best-first expansion of per-depth top-k log-probs
+ *   ddt_compile_visibility  bit-packed [q_len, prefix + q_len] visibility mask
+ *   ddt_verify_attn         tree-verify MLA attention in absorbed form
+ *   ddt_accept              greedy walk: longest accepted chain + bonus token
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) must be device memory of the current CUDA
+ *     device; pointers marked (host) are host memory.  The caller owns all
+ *     memory.  No entry point allocates device memory; split-KV scratch is a
+ *     caller-provided workspace sized by ddt_verify_attn_workspace_size().
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Launches are
+ *     asynchronous on that stream; no entry point synchronises the host except
+ *     ddt_get_error().
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Arguments checkable on the host are checked before any launch; a failure
+ *     returns DDT_ERR_INVALID_ARG / DDT_ERR_UNSUPPORTED / DDT_ERR_WORKSPACE and
+ *     launches nothing.  Inconsistencies only visible in device data (indptr
+ *     not matching budgets, a kv index outside the pool, a tree deeper than
+ *     max_depth, unsorted top-k) are latched by the kernels into a per-device
+ *     error word read back by ddt_get_error(); the offending access is skipped
+ *     (never performed out of bounds) and the affected outputs are unspecified.
+ *   - Launch failures return DDT_ERR_CUDA.
+ */
+#ifndef DDT_H_
+#define DDT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDT_ABI_VERSION 1
+
+/* Sizes fixed by the absorbed-MLA layout ("The 30-Column Mask", shapes log:
+ * Dl=512, Dr=64; "The Forward Pass Pseudocode": scores over c_kv and k_pe,
+ * output in the latent space). */
+#define DDT_DL 512          /* latent width: values, first part of the keys */
+#define DDT_DR 64           /* rope width: second part of the keys */
+#define DDT_D 576           /* row width of q and of the latent KV pool */
+#define DDT_MAX_DEPTH 7     /* draft block of 8 minus the anchor */
+#define DDT_MAX_TOPK 16
+#define DDT_MAX_Q_LEN 128   /* budget + 1 */
+#define DDT_MAX_SPLITS 128
+
+typedef enum {
+    DDT_OK = 0,
+    DDT_ERR_INVALID_ARG = 1,   /* bad pointer / size / shape, found on the host */
+    DDT_ERR_UNSUPPORTED = 2,   /* valid but outside the supported sizes */
+    DDT_ERR_WORKSPACE = 3,     /* workspace missing or too small */
+    DDT_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    DDT_ERR_DEVICE_CHECK = 5,  /* a kernel latched a data check (ddt_get_error) */
+    DDT_ERR_TIMEOUT = 6        /* a bounded device wait gave up (ddt_get_error) */
+} ddt_status;
+
+/* Bits of the device error word (see ddt_get_error). */
+#define DDT_DEVERR_QO_INDPTR    0x001u  /* qo_indptr not matching budget+1 / q_len limits */
+#define DDT_DEVERR_KV_INDPTR    0x002u  /* kv_len < q_len or kv_len > max_kv_len */
+#define DDT_DEVERR_KV_INDEX     0x004u  /* a kv_indices entry outside [0, pool_rows) */
+#define DDT_DEVERR_MASK_INDPTR  0x008u  /* mask_indptr not matching q_len*ceil(kv_len/32) */
+#define DDT_DEVERR_TOPK_ORDER   0x010u  /* top-k log-probs not non-increasing (or NaN) */
+#define DDT_DEVERR_EXHAUSTED    0x020u  /* budget larger than the implicit tree */
+#define DDT_DEVERR_PARENT       0x040u  /* a parent link that is not an earlier node */
+#define DDT_DEVERR_DEPTH        0x080u  /* accepted chain longer than max_depth + 1 */
+#define DDT_DEVERR_TIMEOUT      0x100u  /* a bounded wait inside a kernel ran out */
+
+const char *ddt_status_string(ddt_status s);
+int32_t ddt_abi_version(void);
+
+/*
+ * ddt_build_tree -- best-first tree from per-depth top-k log-probs.
+ * Page: "The DDTree CUDA Graph Fix ..." section "The DDTree Architecture":
+ * pop the highest cumulative-log-prob node, add it, push its best child and
+ * its next sibling, until `budget` nodes are selected; the tree has
+ * budget + 1 nodes (node 0 is the root, the last verified token).
+ *
+ *   topk_logp  (device) float [batch][max_depth][topk]: log-probs of the
+ *              drafter's top-k at draft depth d+1, non-increasing along topk.
+ *   topk_ids   (device) int32 [batch][max_depth][topk]: their token ids.
+ *   root_id    (device) int32 [batch]: token of node 0.
+ *   budget     (device) int32 [batch]: draft nodes to select (0 .. 127).
+ *   qo_indptr  (device) int32 [batch+1]: node offsets, q_len_b = budget_b + 1.
+ *   node_token, parent, depth
+ *              (device) int32 [qo_indptr[batch]] outputs, ragged by qo_indptr:
+ *              parent[root] = -1, depth[root] = 0; nodes appear in pop order,
+ *              so parent[n] < n.
+ * Order among equal scores: smaller depth first, then the path of sibling
+ * ranks compared lexicographically.  Scores are fp32 sums root to leaf.
+ * Supported: 1 <= topk <= 16, 1 <= max_depth <= 7, budget <= 127.
+ */
+ddt_status ddt_build_tree(const float *topk_logp, const int32_t *topk_ids,
+                          const int32_t *root_id, const int32_t *budget,
+                          const int32_t *qo_indptr, int32_t batch, int32_t max_depth,
+                          int32_t topk, int32_t *node_token, int32_t *parent,
+                          int32_t *depth, void *stream);
+
+/*
+ * ddt_mask_indptr -- (host helper) word offsets of the bit-packed mask.
+ * Request b's mask is q_len_b rows of W_b = ceil((prefix_b + q_len_b) / 32)
+ * uint32 words; mask_indptr[b] = sum over b' < b of q_len_b' * W_b'.
+ *   qo_indptr (host) int32 [batch+1]; prefix_len (host) int32 [batch];
+ *   mask_indptr (host) int32 [batch+1] output; returns DDT_ERR_INVALID_ARG on
+ *   negative sizes or int32 overflow.
+ */
+ddt_status ddt_mask_indptr(const int32_t *qo_indptr, const int32_t *prefix_len,
+                           int32_t batch, int32_t *mask_indptr);
+
+/*
+ * ddt_compile_visibility -- the verify mask.
+ * Page: "The DDTree CUDA Graph Fix ..." section "The DDTree Architecture"
+ * (each node attends to its ancestors plus the shared prefix; all prefix
+ * columns visible) and "The 30-Column Mask" section "Mask Stride Formula"
+ * (a row spans prefix + q_len columns: prefix first, then tree node j at
+ * column prefix + j).
+ *
+ *   parent      (device) int32 [qo_indptr[batch]] from ddt_build_tree.
+ *   qo_indptr   (device) int32 [batch+1].
+ *   prefix_len  (device) int32 [batch].
+ *   mask_indptr (device) int32 [batch+1] as given by ddt_mask_indptr.
+ *   total_words = mask_indptr[batch] (host value: the size of `mask`).
+ *   mask        (device) uint32 [total_words] output.  Bit (c mod 32) of word
+ *               c / 32 of row i is column c (LSB first); padding bits are 0.
+ */
+ddt_status ddt_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
+                                  const int32_t *prefix_len, const int32_t *mask_indptr,
+                                  int32_t batch, int32_t total_words, uint32_t *mask,
+                                  void *stream);
+
+/*
+ * Split-KV sizing.  ddt_verify_attn_num_splits() returns the split count the
+ * library would pick for this shape on `num_sms` SMs (num_sms <= 0: query the
+ * current device).  ddt_verify_attn_workspace_size() returns the workspace
+ * bytes ddt_verify_attn needs for `num_splits` splits (0 bytes for one split):
+ * num_splits * total_q * num_heads * (512 + 1) * 4 bytes, 256-byte aligned.
+ */
+int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max_q_len,
+                                   int32_t max_kv_len, int32_t num_sms);
+size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_t num_splits);
+
+/*
+ * ddt_verify_attn -- tree-verify MLA attention, absorbed form.
+ * Pages: "The Architecture of a Speculative Decoding Engine" section "The
+ * Forward Pass Pseudocode" (verify_attn(q_abs, q_pe, c_kv, k_pe, mask, scale)
+ * returning out_latent); "The 30-Column Mask" sections "The Message: Tensor
+ * Shapes as Evidence" and "The Fix: Building Combined Indices" (q = [tokens,
+ * heads, 576], one 576-wide latent row per token shared by all heads, indices
+ * = prefix slots ++ the tree nodes' slots, mask row stride prefix + q_len);
+ * the split-KV partial pass + log-sum-exp combine follows "The 30-Column
+ * Mask" section "The Context: Building a Custom Verify Attention Kernel".
+ *
+ * For row (token t of request b = tree node i, head h):
+ *   s_j  = scale * <q[t,h,0:576], kv_pool[kv_indices[kv_indptr[b]+j], 0:576]>
+ *          over the columns j in [0, kv_len_b) whose mask bit (i, j) is set,
+ *   out[t,h,:] = sum_j softmax(s)_j * kv_pool[...same row..., 0:512],
+ *   lse[t,h]   = log(sum_j exp(s_j))   (natural log).
+ *
+ *   q           (device) bf16 [total_q][num_heads][576] (absorbed q_nope ++ roped q_pe).
+ *   kv_pool     (device) bf16 [pool_rows][576] (c_kv ++ k_pe), 16-byte aligned.
+ *   kv_indices  (device) int32 [kv_indptr[batch]]: per request prefix_len_b
+ *               prefix slots followed by q_len_b tree-node slots in node order.
+ *   kv_indptr   (device) int32 [batch+1]; kv_len_b = prefix_len_b + q_len_b.
+ *   qo_indptr   (device) int32 [batch+1]; q_len_b <= max_q_len <= 128.
+ *   mask, mask_indptr (device) as produced by ddt_compile_visibility.
+ *   total_q     = qo_indptr[batch] (host value); max_q_len / max_kv_len are
+ *               host-side upper bounds used to size the grid.
+ *   num_splits  0 = choose (ddt_verify_attn_num_splits), else 1..128.
+ *   out         (device) float [total_q][num_heads][512].
+ *   lse         (device) float [total_q][num_heads] or NULL.
+ *   workspace   (device) >= ddt_verify_attn_workspace_size(total_q, num_heads,
+ *               splits) bytes, 256-byte aligned; may be NULL when one split.
+ * Supported: num_heads >= 1 (up to 128).
+ */
+ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
+                           const int32_t *kv_indices, const int32_t *kv_indptr,
+                           const int32_t *qo_indptr, const uint32_t *mask,
+                           const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
+                           int32_t total_q, int32_t max_q_len, int32_t max_kv_len, float scale,
+                           int32_t num_splits, float *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * ddt_accept -- greedy tree acceptance (follow_verified_tree).
+ * Page: "The DDTree CUDA Graph Fix ..." section "The DDTree Architecture"
+ * (walk from the root following the target's argmax into the matching child
+ * until none matches; return the longest accepted chain plus one bonus
+ * token); "The Oracle Drafter" section "The Engine Interface Design"
+ * (outputs: accepted path, accept length, commit tokens, bonus);
+ * "The Architecture of a Speculative Decoding Engine" section "The Final
+ * Resolution" (the cache grows by accept_len, which counts the root).
+ *
+ *   node_token, parent (device) int32 [qo_indptr[batch]] (a ddt_build_tree tree).
+ *   qo_indptr     (device) int32 [batch+1].
+ *   target_argmax (device) int32 [qo_indptr[batch]]: target model's argmax at each node.
+ *   accept_len    (device) int32 [batch]: accepted nodes incl. the root (1 .. max_depth+1).
+ *   accepted_nodes(device) int32 [batch][max_depth+1]: node indices, -1 padded.
+ *   commit_tokens (device) int32 [batch][max_depth+1]: accepted draft tokens then
+ *                 the bonus token (accept_len entries), -1 padded.
+ *   bonus         (device) int32 [batch]: target argmax at the last accepted node.
+ * Among children carrying the same token the lowest node index is followed.
+ */
+ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
+                      const int32_t *qo_indptr, const int32_t *target_argmax, int32_t batch,
+                      int32_t max_depth, int32_t *accept_len, int32_t *accepted_nodes,
+                      int32_t *commit_tokens, int32_t *bonus, void *stream);
+
+/*
+ * ddt_get_error -- read and clear the current device's error word.
+ * Synchronises `stream`, copies the word to *device_error (host; may be NULL)
+ * and resets it.  Returns DDT_OK when the word was 0, DDT_ERR_TIMEOUT when the
+ * timeout bit was set, DDT_ERR_DEVICE_CHECK for any other bit, DDT_ERR_CUDA
+ * when the copy failed.
+ */
+ddt_status ddt_get_error(void *stream, uint32_t *device_error);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DDT_H_ */

@@ -1,0 +1,106 @@
+"""The C ABI library without a GPU: it loads, exports every declared entry
+point, and its host-side logic (mask layout, workspace sizing, argument
+checks) behaves as documented.  No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ddt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tree_speculative_decoding_gb300 import _build
+    _build.build()
+    from tree_speculative_decoding_gb300 import ddt
+    return ddt.lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ddt_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    exported = set(re.findall(r" T (ddt_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.ddt_abi_version() == 1
+    assert lib.ddt_status_string(0) == b"ok"
+    assert b"workspace" in lib.ddt_status_string(3)
+
+
+def test_mask_indptr_matches_oracle(lib, oracle_mod):
+    from tree_speculative_decoding_gb300 import ddt
+    import torch
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        B = int(rng.integers(1, 40))
+        T = rng.integers(1, 129, B)
+        P = rng.integers(0, 20000, B)
+        qo = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
+        got = ddt.ddt_mask_indptr(torch.from_numpy(qo), torch.from_numpy(P.astype(np.int32)))
+        ref = oracle_mod.mask_indptr(qo, P.astype(np.int32))
+        assert got.numpy().tolist() == ref.tolist()
+
+
+def test_mask_indptr_rejects_bad_sizes(lib):
+    qo = (ctypes.c_int32 * 3)(0, 5, 5)          # second request has q_len 0
+    pl = (ctypes.c_int32 * 2)(3, 4)
+    out = (ctypes.c_int32 * 3)()
+    assert lib.ddt_mask_indptr(qo, pl, 2, out) == 1
+    assert lib.ddt_mask_indptr(None, pl, 2, out) == 1
+
+
+def test_workspace_size_formula(lib):
+    assert lib.ddt_verify_attn_workspace_size(33, 64, 1) == 0
+    rows = 33 * 64
+    a = (rows * 4 * 512 * 4 + 255) // 256 * 256
+    b = (rows * 4 * 4 + 255) // 256 * 256
+    assert lib.ddt_verify_attn_workspace_size(33, 64, 4) == a + b
+
+
+def test_num_splits_is_bounded(lib):
+    for B, H, T, N in [(1, 64, 33, 4129), (8, 64, 33, 16417), (1, 8, 9, 30), (1, 64, 65, 131137),
+                       (32, 16, 33, 8225)]:
+        s = lib.ddt_verify_attn_num_splits(B, H, T, N, 148)
+        assert 1 <= s <= 128
+        assert s == 1 or N // s >= 64
+
+
+def test_host_argument_checks_launch_nothing(lib):
+    dummy = ctypes.c_void_p(16)
+    # null pointers -> invalid argument, returned before any CUDA call
+    assert lib.ddt_build_tree(None, dummy, dummy, dummy, dummy, 1, 7, 8, dummy, dummy, dummy,
+                              None) == 1
+    # unsupported sizes
+    assert lib.ddt_build_tree(dummy, dummy, dummy, dummy, dummy, 1, 8, 8, dummy, dummy, dummy,
+                              None) == 2
+    assert lib.ddt_build_tree(dummy, dummy, dummy, dummy, dummy, 1, 7, 17, dummy, dummy, dummy,
+                              None) == 2
+    assert lib.ddt_accept(dummy, dummy, dummy, dummy, 1, 0, dummy, dummy, dummy, dummy, None) == 2
+    assert lib.ddt_compile_visibility(None, dummy, dummy, dummy, 1, 10, dummy, None) == 1
+    args = [dummy, dummy, 100, dummy, dummy, dummy, dummy, dummy]
+    #        B  H   total_q max_q max_kv scale splits
+    bad = [(0, 8, 9, 9, 30, 0.1, 0), (1, 8, 9, 9, 5, 0.1, 0), (1, 8, 9, 9, 30, float("nan"), 0),
+           (1, 8, 9, 9, 30, 0.1, -1)]
+    for B, H, tq, mq, mk, sc, sp in bad:
+        assert lib.ddt_verify_attn(*args, B, H, tq, mq, mk, sc, sp, dummy, None, None, 0,
+                                   None) == 1
+    assert lib.ddt_verify_attn(*args, 1, 8, 129, 129, 300, 0.1, 0, dummy, None, None, 0, None) == 2
+    assert lib.ddt_verify_attn(*args, 1, 129, 9, 9, 30, 0.1, 0, dummy, None, None, 0, None) == 2
+    # misaligned kv_pool
+    a2 = [dummy, ctypes.c_void_p(18), 100, dummy, dummy, dummy, dummy, dummy]
+    assert lib.ddt_verify_attn(*a2, 1, 8, 9, 9, 30, 0.1, 0, dummy, None, None, 0, None) == 1

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tree, mask and accept must match bit for bit.  Attention must satisfy
+max|diff| <= 1e-2 * max|ref| and mean relative error (sum|diff| / sum|ref|)
+<= 2e-3 against the fp64 oracle (bf16 inputs, fp32 accumulation and output).
+Small workloads compare every row; the full-size ones compare sampled rows
+the oracle computes one by one, plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_speculative_decoding_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL = 1e-2
+MEAN_TOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tree_speculative_decoding_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def _step(wl, argmax=None, num_splits=0):
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    st = VerifyStep(wl, "cuda:0", target_argmax=argmax, num_splits=num_splits)
+    st.run()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    return st
+
+
+def _oracle_tree(wl):
+    return oracle.build_tree(wl.topk_logp, wl.topk_ids, wl.root_id, wl.budget, wl.qo_indptr,
+                             wl.max_depth, wl.K)
+
+
+def _sample_rows(wl, n, seed=0):
+    rows_total = wl.total_q * wl.H
+    if n >= rows_total:
+        return np.arange(rows_total, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    picks = set()
+    for b in range(wl.B):   # first and last node of every request, a random head
+        for t in (wl.qo_indptr[b], wl.qo_indptr[b + 1] - 1):
+            picks.add(int(t) * wl.H + int(rng.integers(wl.H)))
+    while len(picks) < n:
+        picks.add(int(rng.integers(rows_total)))
+    return np.array(sorted(picks), dtype=np.int64)
+
+
+def _check_attn(st, wl, mask, mip, rows):
+    ref, ref_lse = oracle.verify_attn(wl.q, wl.kv_pool, wl.kv_indices, wl.kv_indptr,
+                                      wl.qo_indptr, mask, mip, wl.H, wl.scale, rows=rows)
+    out = st.out.reshape(-1, 512)
+    got = out[torch.from_numpy(rows).to(out.device)].double().cpu().numpy()
+    got_lse = st.lse.reshape(-1)[torch.from_numpy(rows).to(out.device)].double().cpu().numpy()
+    diff = np.abs(got - ref)
+    assert diff.max() <= MAX_TOL * np.abs(ref).max(), f"max|diff| {diff.max()}"
+    assert diff.sum() / np.abs(ref).sum() <= MEAN_TOL, f"mean rel {diff.sum() / np.abs(ref).sum()}"
+    np.testing.assert_allclose(got_lse, ref_lse, rtol=1e-4, atol=1e-3)
+    full = st.out
+    assert torch.isfinite(full).all() and torch.isfinite(st.lse).all()
+    return diff.max() / np.abs(ref).max()
+
+
+def _full_check(wl, n_rows, argmax=None, num_splits=0):
+    st = _step(wl, argmax=argmax, num_splits=num_splits)
+    tok, par, dep = _oracle_tree(wl)
+    np.testing.assert_array_equal(st.node_token.cpu().numpy(), tok)
+    np.testing.assert_array_equal(st.parent.cpu().numpy(), par)
+    np.testing.assert_array_equal(st.depth.cpu().numpy(), dep)
+    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    np.testing.assert_array_equal(st.mask.cpu().numpy().view(np.uint32), mask)
+    np.testing.assert_array_equal(st.mask_indptr_host.numpy(), mip)
+    _check_attn(st, wl, mask, mip, _sample_rows(wl, n_rows))
+    am = wl.argmax_random if argmax is None else argmax
+    alen, acc, com, bon = oracle.accept(tok, par, wl.qo_indptr, am, wl.max_depth)
+    np.testing.assert_array_equal(st.accept_len.cpu().numpy(), alen)
+    np.testing.assert_array_equal(st.accepted_nodes.cpu().numpy(), acc)
+    np.testing.assert_array_equal(st.commit_tokens.cpu().numpy(), com)
+    np.testing.assert_array_equal(st.bonus.cpu().numpy(), bon)
+    return st, (tok, par, dep)
+
+
+def test_tiny_shapes_log_workload():
+    _full_check(workloads.preset("tiny_p21_b8_h8"), n_rows=10 ** 9)
+
+
+def test_single_request_full_heads():
+    _full_check(workloads.preset("single_p4096_b32_h64"), n_rows=512)
+
+
+def test_ragged_batch():
+    _full_check(workloads.preset("ragged_bs8_b32_h64"), n_rows=160)
+
+
+def test_long_context_split_kv():
+    wl = workloads.preset("long_p131072_b64_h64")
+    st, _ = _full_check(wl, n_rows=48)
+    assert st.num_splits > 1
+
+
+def test_mixed_budgets_with_half_matching_targets():
+    wl = workloads.preset("mixed_bs32_b16or32_h16")
+    tok, par, _ = _oracle_tree(wl)
+    argmax = oracle.best_child_argmax(par, wl.qo_indptr, tok, wl.argmax_coin, wl.argmax_random)
+    st, _ = _full_check(wl, n_rows=256, argmax=argmax)
+    assert st.accept_len.max().item() > 1   # the 50% matches do get accepted
+
+
+def test_chain_forcing_targets_accept_deep_paths():
+    wl = workloads.preset("single_p4096_b32_h64")
+    tok, par, _ = _oracle_tree(wl)
+    coin = np.ones(wl.total_q, np.uint8)
+    argmax = oracle.best_child_argmax(par, wl.qo_indptr, tok, coin, wl.argmax_random)
+    st, _ = _full_check(wl, n_rows=64, argmax=argmax)
+    assert st.accept_len.item() >= 2
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
+def test_forced_split_counts_agree(splits):
+    wl = workloads.make_workload("splits", 99, 2, 16, [700, 1500], [20, 5], 4, 1000, 2.0)
+    _full_check(wl, n_rows=10 ** 9, num_splits=splits)
+
+
+@pytest.mark.parametrize("H", [1, 3, 16, 17, 128])
+def test_head_counts(H):
+    wl = workloads.make_workload(f"h{H}", 500 + H, 2, H, [64, 33], [9, 3], 3, 200, 1.5)
+    _full_check(wl, n_rows=10 ** 9)
+
+
+def test_degenerate_requests_prefix0_budget0_and_max_qlen():
+    # prefix 0 (the root sees only itself), budget 0 (plain autoregressive
+    # verify: q_len 1) and the largest tree (budget 127, q_len 128)
+    wl = workloads.make_workload("edge", 4242, 4, 8, [0, 57, 1, 300], [5, 0, 127, 31], 16, 5000,
+                                 1.0)
+    _full_check(wl, n_rows=10 ** 9)
+
+
+def test_chain_tree_equals_causal_prefill():
+    wl = workloads.make_workload("chain", 77, 1, 4, [40], [7], 1, 300, 2.0)
+    st, (tok, par, dep) = _full_check(wl, n_rows=10 ** 9)
+    assert dep.tolist() == list(range(8))
+
+
+def test_cuda_graph_capture_and_replay():
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("graph", 31, 3, 16, [500, 20, 1100], [16, 9, 32], 8, 3000, 2.0)
+    st = VerifyStep(wl, "cuda:0")
+    st.run()
+    torch.cuda.synchronize()
+    ref_out = st.out.clone()
+    ref_tok = st.node_token.clone()
+    st.out.zero_()
+    st.node_token.fill_(-9)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            st.run(stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    assert torch.equal(st.node_token, ref_tok)
+    assert torch.equal(st.out, ref_out)
+
+
+def test_out_of_range_kv_index_is_latched_not_faulted():
+    from tree_speculative_decoding_gb300 import ddt
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("bad", 5, 1, 8, [100], [4], 2, 100, 1.0)
+    st = VerifyStep(wl, "cuda:0")
+    st.kv_indices[7] = wl.pool_rows + 1000   # made on the host, caught by the kernel's check
+    st.run()
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 5 and bits & 0x4
+    assert ddt.ddt_get_error() == (0, 0)     # cleared
+
+
+def test_wrong_mask_stride_is_rejected():
+    # the 30-column mask bug: a mask laid out with stride kv_len_max (prefix
+    # only) instead of prefix + q_len must not be consumed silently
+    from tree_speculative_decoding_gb300 import ddt
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("stride", 6, 1, 8, [21], [8], 4, 512, 2.0)
+    st = VerifyStep(wl, "cuda:0")
+    st.run()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    T, P = 9, 21
+    bad = torch.tensor([0, T * ((P + 31) // 32 + 1)], dtype=torch.int32, device="cuda:0")
+    ddt.ddt_verify_attn(st.q, st.kv_pool, st.kv_indices, st.kv_indptr, st.qo_indptr, st.mask,
+                        bad, wl.scale, st.out, st.lse, max_q_len=9, max_kv_len=30)
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 5 and bits & 0x8
+
+
+def test_bad_budget_indptr_is_latched():
+    from tree_speculative_decoding_gb300 import ddt
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("budget", 8, 2, 4, [10, 10], [3, 3], 2, 50, 1.0)
+    st = VerifyStep(wl, "cuda:0")
+    st.budget[1] = 4                         # disagrees with qo_indptr
+    st.build_tree()
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 5 and bits & 0x1

@@ -1,0 +1,45 @@
+"""The N>1 bench path on CPU: two gloo ranks, each with its own replica of the
+work, reduce to (max elapsed, summed units) exactly as bench.py does."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    elapsed, units = bench.reduce_over_ranks(1.5 + rank, 10.0 * (rank + 1), dist)
+    q.put((rank, elapsed, units))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_reduction():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2.5, 30.0), (1, 2.5, 30.0)]
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.reduce_over_ranks(3.0, 7.0, None) == (3.0, 7.0)

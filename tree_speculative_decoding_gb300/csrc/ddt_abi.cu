@@ -1,0 +1,250 @@
+// ddt_abi.cu -- the extern "C" entry points of libddt.so: host-side argument
+// checks, split-KV sizing, launches, and the per-device error word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "ddt_internal.cuh"
+
+namespace {
+
+// Per-device error word: kernels atomicOr DDT_DEVERR_* bits into it.
+__device__ unsigned int g_ddt_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    unsigned int *err = nullptr;  // device address of g_ddt_error_word
+    int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Set up (once per device, with that device current) the error-word address,
+// the SM count and kernel attributes.  The first entry-point call on a device
+// performs this set-up, so it should come before any stream capture.  Returns
+// null on failure.
+DeviceState *device_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceState &st = g_dev[dev];
+    if (st.ready) return &st;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!st.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ddt_error_word) != cudaSuccess) return nullptr;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        if (ddt::attn_prepare_device() != cudaSuccess) return nullptr;
+        st.err = static_cast<unsigned int *>(p);
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    return &st;
+}
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
+    // CTAs without splitting: one per (request, node, 16-head group)
+    const long long ctas = (long long)batch * max_q_len * ((num_heads + 15) / 16);
+    const long long target = 2LL * num_sms;
+    long long splits = (target + ctas - 1) / ctas;
+    const long long by_len = max_kv_len / 256;  // keep >= 256 columns per split
+    if (splits > by_len) splits = by_len;
+    if (splits < 1) splits = 1;
+    if (splits > DDT_MAX_SPLITS) splits = DDT_MAX_SPLITS;
+    return (int)splits;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ddt_status_string(ddt_status s) {
+    switch (s) {
+        case DDT_OK: return "ok";
+        case DDT_ERR_INVALID_ARG: return "invalid argument";
+        case DDT_ERR_UNSUPPORTED: return "unsupported size";
+        case DDT_ERR_WORKSPACE: return "workspace missing or too small";
+        case DDT_ERR_CUDA: return "CUDA error";
+        case DDT_ERR_DEVICE_CHECK: return "device-side data check failed";
+        case DDT_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t ddt_abi_version(void) { return DDT_ABI_VERSION; }
+
+ddt_status ddt_build_tree(const float *topk_logp, const int32_t *topk_ids,
+                          const int32_t *root_id, const int32_t *budget,
+                          const int32_t *qo_indptr, int32_t batch, int32_t max_depth,
+                          int32_t topk, int32_t *node_token, int32_t *parent, int32_t *depth,
+                          void *stream) {
+    if (!topk_logp || !topk_ids || !root_id || !budget || !qo_indptr || !node_token ||
+        !parent || !depth || batch < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH || topk < 1 || topk > DDT_MAX_TOPK)
+        return DDT_ERR_UNSUPPORTED;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_build_tree(topk_logp, topk_ids, root_id, budget, qo_indptr, batch,
+                                           max_depth, topk, node_token, parent, depth, st->err,
+                                           as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+ddt_status ddt_mask_indptr(const int32_t *qo_indptr, const int32_t *prefix_len, int32_t batch,
+                           int32_t *mask_indptr) {
+    if (!qo_indptr || !prefix_len || !mask_indptr || batch < 0) return DDT_ERR_INVALID_ARG;
+    int64_t off = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t T = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        const int64_t P = prefix_len[b];
+        if (T < 1 || P < 0) return DDT_ERR_INVALID_ARG;
+        mask_indptr[b] = (int32_t)off;
+        off += T * ((P + T + 31) / 32);
+        if (off > INT32_MAX) return DDT_ERR_INVALID_ARG;
+    }
+    mask_indptr[batch] = (int32_t)off;
+    return DDT_OK;
+}
+
+ddt_status ddt_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
+                                  const int32_t *prefix_len, const int32_t *mask_indptr,
+                                  int32_t batch, int32_t total_words, uint32_t *mask,
+                                  void *stream) {
+    if (!parent || !qo_indptr || !prefix_len || !mask_indptr || !mask || batch < 0 ||
+        total_words < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (batch == 0 || total_words == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_compile_visibility(parent, qo_indptr, prefix_len, mask_indptr,
+                                                   batch, total_words, mask, st->err,
+                                                   as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max_q_len,
+                                   int32_t max_kv_len, int32_t num_sms) {
+    if (batch < 1 || num_heads < 1 || max_q_len < 1 || max_kv_len < 1) return 1;
+    if (num_sms <= 0) {
+        DeviceState *st = device_state();
+        num_sms = st ? st->num_sms : 148;
+    }
+    return choose_splits(batch, num_heads, max_q_len, max_kv_len, num_sms);
+}
+
+size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_t num_splits) {
+    if (total_q < 1 || num_heads < 1 || num_splits <= 1) return 0;
+    const size_t rows = (size_t)total_q * num_heads;
+    return align256(rows * num_splits * DDT_DL * sizeof(float)) +
+           align256(rows * num_splits * sizeof(float));
+}
+
+ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
+                           const int32_t *kv_indices, const int32_t *kv_indptr,
+                           const int32_t *qo_indptr, const uint32_t *mask,
+                           const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
+                           int32_t total_q, int32_t max_q_len, int32_t max_kv_len, float scale,
+                           int32_t num_splits, float *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (!q || !kv_pool || !kv_indices || !kv_indptr || !qo_indptr || !mask || !mask_indptr ||
+        !out)
+        return DDT_ERR_INVALID_ARG;
+    if (batch < 1 || num_heads < 1 || total_q < batch || pool_rows < 1 || max_q_len < 1 ||
+        max_kv_len < max_q_len || !isfinite(scale) || num_splits < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (max_q_len > DDT_MAX_Q_LEN || num_heads > 128 || num_splits > DDT_MAX_SPLITS)
+        return DDT_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(kv_pool) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u) ||
+        (reinterpret_cast<uintptr_t>(out) & 15u))
+        return DDT_ERR_INVALID_ARG;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+
+    int splits = num_splits > 0
+        ? num_splits
+        : choose_splits(batch, num_heads, max_q_len, max_kv_len, st->num_sms);
+    const int tile = ddt::attn_kv_tile();
+    int split_cols = (max_kv_len + splits - 1) / splits;
+    split_cols = (split_cols + tile - 1) / tile * tile;
+    splits = (max_kv_len + split_cols - 1) / split_cols;  // no empty tail splits
+
+    ddt::AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = q;
+    a.kv_pool = kv_pool;
+    a.pool_rows = pool_rows;
+    a.kv_indices = kv_indices;
+    a.kv_indptr = kv_indptr;
+    a.qo_indptr = qo_indptr;
+    a.mask = mask;
+    a.mask_indptr = mask_indptr;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.total_q = total_q;
+    a.max_q_len = max_q_len;
+    a.max_kv_len = max_kv_len;
+    a.scale = scale;
+    a.num_splits = splits;
+    a.split_cols = split_cols;
+    a.out = out;
+    a.lse = lse;
+    a.err = st->err;
+    if (splits > 1) {
+        const size_t need = ddt_verify_attn_workspace_size(total_q, num_heads, splits);
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return DDT_ERR_WORKSPACE;
+        const size_t rows = (size_t)total_q * num_heads;
+        a.o_part = static_cast<float *>(workspace);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align256(rows * splits * DDT_DL * sizeof(float)));
+    }
+    cudaStream_t s = as_stream(stream);
+    cudaError_t e = ddt::launch_attn_partial(a, s);
+    if (e == cudaSuccess && splits > 1) e = ddt::launch_attn_combine(a, s);
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
+                      const int32_t *qo_indptr, const int32_t *target_argmax, int32_t batch,
+                      int32_t max_depth, int32_t *accept_len, int32_t *accepted_nodes,
+                      int32_t *commit_tokens, int32_t *bonus, void *stream) {
+    if (!node_token || !parent || !qo_indptr || !target_argmax || !accept_len ||
+        !accepted_nodes || !commit_tokens || !bonus || batch < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH) return DDT_ERR_UNSUPPORTED;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_accept(node_token, parent, qo_indptr, target_argmax, batch,
+                                       max_depth, accept_len, accepted_nodes, commit_tokens,
+                                       bonus, st->err, as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+ddt_status ddt_get_error(void *stream, uint32_t *device_error) {
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaStream_t s = as_stream(stream);
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, st->err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(st->err, 0, sizeof word, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DDT_ERR_CUDA;
+    if (device_error) *device_error = word;
+    if (word == 0) return DDT_OK;
+    return (word & DDT_DEVERR_TIMEOUT) ? DDT_ERR_TIMEOUT : DDT_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

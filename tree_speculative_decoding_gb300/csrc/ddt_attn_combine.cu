@@ -1,0 +1,63 @@
+// ddt_attn_combine.cu -- log-sum-exp merge of split-KV partial results.
+//
+// Each split s wrote, for every row (token, head), its normalised partial
+// output o_s = sum_j e^{s_j - m_s} v_j / sum_j e^{s_j - m_s} and
+// lse_s = log sum_j e^{s_j} over its own kv columns.  The full softmax over
+// the union of the splits is  out = sum_s e^{lse_s - LSE} o_s  with
+// LSE = log sum_s e^{lse_s}.  A split that saw no visible column carries
+// lse_s = -inf and contributes nothing.
+// Split-KV with a partial reduction follows "The 30-Column Mask", section
+// "The Context: Building a Custom Verify Attention Kernel" (a KV-split
+// flash-decode design with partial reduction for occupancy).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "ddt_internal.cuh"
+
+namespace ddt {
+namespace {
+
+constexpr int kThreads = 128;  // 4 output dims per thread
+
+__global__ void __launch_bounds__(kThreads)
+attn_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
+                    int num_splits, int64_t rows, float *__restrict__ out,
+                    float *__restrict__ lse) {
+    const int64_t row = blockIdx.x;
+    if (row >= rows) return;
+    float m = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[(int64_t)s * rows + row]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (m != -INFINITY) {
+        for (int s = 0; s < num_splits; ++s) {
+            const float ls = lse_part[(int64_t)s * rows + row];
+            if (ls == -INFINITY) continue;
+            const float w = __expf(ls - m);
+            den += w;
+            const float4 o = reinterpret_cast<const float4 *>(
+                o_part + ((int64_t)s * rows + row) * DDT_DL)[threadIdx.x];
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+        const float inv = 1.f / den;
+        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    }
+    reinterpret_cast<float4 *>(out + row * DDT_DL)[threadIdx.x] = acc;
+    if (lse && threadIdx.x == 0) lse[row] = (m == -INFINITY) ? -INFINITY : m + logf(den);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s) {
+    const int64_t rows = (int64_t)a.total_q * a.num_heads;
+    if (rows == 0) return cudaSuccess;
+    attn_combine_kernel<<<(unsigned)rows, kThreads, 0, s>>>(a.o_part, a.lse_part, a.num_splits,
+                                                            rows, a.out, a.lse);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

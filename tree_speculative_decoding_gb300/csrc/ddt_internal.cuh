@@ -1,0 +1,70 @@
+// ddt_internal.cuh -- declarations shared by the CUDA translation units of
+// libddt.so (launchers defined in each .cu, called from ddt_abi.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ddt.h"
+
+namespace ddt {
+
+// Latch a device-side check into the per-device error word.
+__device__ __forceinline__ void latch(unsigned int *err, unsigned int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// Launchers (host functions; each enqueues on `s` and returns the launch error).
+cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
+                              const int32_t *root_id, const int32_t *budget,
+                              const int32_t *qo_indptr, int batch, int max_depth, int topk,
+                              int32_t *node_token, int32_t *parent, int32_t *depth,
+                              unsigned int *err, cudaStream_t s);
+
+cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
+                                      const int32_t *prefix_len, const int32_t *mask_indptr,
+                                      int batch, int total_words, uint32_t *mask,
+                                      unsigned int *err, cudaStream_t s);
+
+cudaError_t launch_accept(const int32_t *node_token, const int32_t *parent,
+                          const int32_t *qo_indptr, const int32_t *target_argmax, int batch,
+                          int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
+                          int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
+                          cudaStream_t s);
+
+// Arguments of one verify-attention call as seen by the kernels.
+struct AttnArgs {
+    const uint16_t *q;
+    const uint16_t *kv_pool;
+    int64_t pool_rows;
+    const int32_t *kv_indices;
+    const int32_t *kv_indptr;
+    const int32_t *qo_indptr;
+    const uint32_t *mask;
+    const int32_t *mask_indptr;
+    int batch;
+    int num_heads;
+    int total_q;
+    int max_q_len;
+    int max_kv_len;
+    float scale;
+    int num_splits;
+    int split_cols;       // kv columns per split (multiple of the kv tile)
+    float *out;           // [total_q, H, 512]
+    float *lse;           // [total_q, H] or null
+    float *o_part;        // [splits, total_q*H, 512] when num_splits > 1
+    float *lse_part;      // [splits, total_q*H]
+    unsigned int *err;
+};
+
+cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
+
+// kv columns per split must be a multiple of this (the attention kv tile)
+int attn_kv_tile();
+
+// Once per device, with that device current and before any stream capture:
+// kernel attributes (dynamic shared memory opt-in).
+cudaError_t attn_prepare_device();
+
+}  // namespace ddt

@@ -1,0 +1,320 @@
+// ddt_tree.cu -- the three small stages of the verify step: best-first tree
+// build, visibility-mask compile and greedy accept.  One warp per request for
+// the sequential walks, one thread per mask word for the mask.
+//
+// Page: "The DDTree CUDA Graph Fix: Unlocking Speculative Decoding at 109 tok/s
+// on PCIe Blackwell", section "The DDTree Architecture: Confirming
+// Multiple-Path Evaluation" (heap expansion, ancestor-plus-prefix visibility,
+// follow-the-argmax acceptance with one bonus token).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ddt_internal.cuh"
+
+namespace ddt {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int SLOTS = 4;  // frontier slots per lane: 32 x 4 = 128 >= budget + 1
+
+// Candidate key: larger key pops first.
+//   bits 63..32  score mapped to an order-preserving uint32 (higher score first)
+//   bits 31..29  7 - depth                    (shallower first on equal score)
+//   bits 27..0   0x0FFFFFFF - rank path       (lexicographically smaller first)
+// The rank path packs the sibling rank at depth k into bits 27-4(k-1)..24-4(k-1),
+// so equal-depth paths compare lexicographically as integers.  Keys of distinct
+// nodes are distinct, and 0 marks an empty slot (a real key is never 0: its
+// high word is at least 0x007FFFFF).
+__device__ __forceinline__ uint32_t order_score(float f) {
+    f = f + 0.0f;  // -0 -> +0 so that equal scores give equal keys
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unorder_score(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+__device__ __forceinline__ uint64_t make_key(float score, int depth, uint32_t path) {
+    return ((uint64_t)order_score(score) << 32) | ((uint64_t)(7 - depth) << 29) |
+           (uint64_t)(0x0FFFFFFFu - path);
+}
+__device__ __forceinline__ int key_depth(uint64_t k) { return 7 - (int)((k >> 29) & 7u); }
+__device__ __forceinline__ uint32_t key_path(uint64_t k) {
+    return 0x0FFFFFFFu - (uint32_t)(k & 0x0FFFFFFFu);
+}
+__device__ __forceinline__ int path_rank(uint32_t path, int depth) {  // rank at `depth`
+    return (int)((path >> (28 - 4 * depth)) & 0xFu);
+}
+
+// One warp per request.  The frontier (candidates not yet popped) lives in
+// registers, SLOTS entries per lane; each pop is a warp-wide max.
+__global__ void __launch_bounds__(32)
+build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict__ topk_ids,
+                  const int32_t *__restrict__ root_id, const int32_t *__restrict__ budget,
+                  const int32_t *__restrict__ qo_indptr, int max_depth, int K,
+                  int32_t *__restrict__ node_token, int32_t *__restrict__ parent,
+                  int32_t *__restrict__ depth, unsigned int *err) {
+    __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x;
+    const float *lpb = topk_logp + (size_t)b * max_depth * K;
+    const int32_t *idb = topk_ids + (size_t)b * max_depth * K;
+
+    bool sorted_ok = true;
+    for (int e = lane; e < max_depth * K; e += 32) {
+        float v = lpb[e];
+        lp[e] = v;
+        if ((e % K) > 0 && !(v <= lpb[e - 1])) sorted_ok = false;  // also rejects NaN
+        if ((e % K) == 0 && v != v) sorted_ok = false;
+    }
+    __syncwarp();
+    if (__any_sync(FULL, !sorted_ok)) {
+        if (lane == 0) latch(err, DDT_DEVERR_TOPK_ORDER);
+        return;
+    }
+
+    const int base = qo_indptr[b];
+    const int nb = budget[b];
+    if (nb < 0 || nb > DDT_MAX_Q_LEN - 1 || qo_indptr[b + 1] - base != nb + 1) {
+        if (lane == 0) latch(err, DDT_DEVERR_QO_INDPTR);
+        return;
+    }
+    if (lane == 0) {
+        node_token[base] = root_id[b];
+        parent[base] = -1;
+        depth[base] = 0;
+    }
+    if (nb == 0) return;
+
+    uint64_t key[SLOTS];
+    float pscore[SLOTS];  // score of the candidate's parent (for its next sibling)
+    int pout[SLOTS];      // output index of the candidate's parent
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) { key[s] = 0; pscore[s] = 0.f; pout[s] = 0; }
+    if (lane == 0) {  // seed: rank-0 child of the root
+        key[0] = make_key(0.0f + lp[0], 1, 0u);
+        pscore[0] = 0.0f;
+        pout[0] = 0;
+    }
+
+    for (int n = 1; n <= nb; ++n) {
+        // lane-local best
+        uint64_t best = 0;
+        int bs = 0;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+            if (key[s] > best) { best = key[s]; bs = s; }
+        const uint32_t hi = (uint32_t)(best >> 32);
+        const uint32_t mhi = __reduce_max_sync(FULL, hi);
+        if (mhi == 0u) {  // frontier empty: budget exceeds the implicit tree
+            if (lane == 0) latch(err, DDT_DEVERR_EXHAUSTED);
+            return;
+        }
+        const uint32_t lo = (uint32_t)best;
+        const uint32_t mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
+        const unsigned who = __ballot_sync(FULL, hi == mhi && lo == mlo && best != 0);
+        const int wl = __ffs(who) - 1;
+
+        // winner pops its slot; the sibling (same parent) reuses that slot
+        int cd = 0, has_child = 0;
+        float cscore = 0.f;
+        uint32_t cpath = 0;
+        if (lane == wl) {
+            const int d = key_depth(best);
+            const uint32_t path = key_path(best);
+            const int r = path_rank(path, d);
+            const float score = unorder_score(mhi);
+            int my_pout = 0;
+            float my_pscore = 0.f;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+                if (s == bs) { my_pout = pout[s]; my_pscore = pscore[s]; }
+            node_token[base + n] = idb[(d - 1) * K + r];
+            parent[base + n] = my_pout;
+            depth[base + n] = d;
+            uint64_t sib = 0;  // next sibling: same parent, so pscore / pout stay
+            if (r + 1 < K)
+                sib = make_key(my_pscore + lp[(d - 1) * K + r + 1], d,
+                               path + (1u << (28 - 4 * d)));
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+                if (s == bs) key[s] = sib;
+            if (d < max_depth) {
+                has_child = 1;
+                cd = d + 1;
+                cscore = score + lp[d * K + 0];
+                cpath = path;  // rank 0 at the new depth
+            }
+        }
+        has_child = __shfl_sync(FULL, has_child, wl);
+        if (has_child && n < nb) {
+            cd = __shfl_sync(FULL, cd, wl);
+            const float parent_score = __shfl_sync(FULL, unorder_score(mhi), wl);
+            cscore = __shfl_sync(FULL, cscore, wl);
+            cpath = __shfl_sync(FULL, cpath, wl);
+            // first lane with a free slot takes the child
+            int free_slot = -1;
+#pragma unroll
+            for (int s = SLOTS - 1; s >= 0; --s)
+                if (key[s] == 0) free_slot = s;
+            const unsigned has_free = __ballot_sync(FULL, free_slot >= 0);
+            const int tl = __ffs(has_free) - 1;  // exists: frontier <= budget < 128
+            if (lane == tl) {
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s)
+                    if (s == free_slot) {
+                        key[s] = make_key(cscore, cd, cpath);
+                        pscore[s] = parent_score;
+                        pout[s] = n;
+                    }
+            }
+        }
+    }
+}
+
+// One thread per mask word (grid-stride).  Word w of request b: row
+// i = local / W_b, columns [32k, 32k+32) with k = local % W_b.
+__global__ void compile_visibility_kernel(const int32_t *__restrict__ parent,
+                                          const int32_t *__restrict__ qo_indptr,
+                                          const int32_t *__restrict__ prefix_len,
+                                          const int32_t *__restrict__ mask_indptr, int batch,
+                                          int total_words, uint32_t *__restrict__ mask,
+                                          unsigned int *err) {
+    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < total_words;
+         w += gridDim.x * blockDim.x) {
+        // request owning word w: last b with mask_indptr[b] <= w
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (mask_indptr[mid] <= w) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int T = qo_indptr[b + 1] - qo_indptr[b];
+        const int P = prefix_len[b];
+        const int N = P + T;
+        const int W = (N + 31) >> 5;
+        if (T < 1 || T > DDT_MAX_Q_LEN || P < 0 ||
+            mask_indptr[b + 1] - mask_indptr[b] != T * W) {
+            latch(err, DDT_DEVERR_MASK_INDPTR);
+            mask[w] = 0u;
+            continue;
+        }
+        const int local = w - mask_indptr[b];
+        const int i = local / W;
+        const int k = local - i * W;
+        const int c0 = k * 32;
+        uint32_t bits = 0u;
+        // prefix columns [c0, min(c0+32, P))
+        if (c0 < P) {
+            const int n = min(32, P - c0);
+            bits = (n == 32) ? 0xffffffffu : ((1u << n) - 1u);
+        }
+        // tree columns: node i and its ancestors
+        if (c0 + 32 > P && c0 < N) {
+            const int32_t *par = parent + qo_indptr[b];
+            int j = i, guard = 0;
+            while (j >= 0) {
+                const int c = P + j;
+                if (c >= c0 && c < c0 + 32) bits |= 1u << (c - c0);
+                const int pj = par[j];
+                if (pj >= j || ++guard > DDT_MAX_Q_LEN) {  // parents must precede
+                    if (pj >= 0) latch(err, DDT_DEVERR_PARENT);
+                    break;
+                }
+                j = pj;
+            }
+        }
+        mask[w] = bits;
+    }
+}
+
+// One warp per request: walk from the root into the child carrying the
+// target's argmax; lanes scan the nodes, the lowest matching index wins.
+__global__ void __launch_bounds__(32)
+accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict__ parent,
+              const int32_t *__restrict__ qo_indptr, const int32_t *__restrict__ target_argmax,
+              int max_depth, int32_t *__restrict__ accept_len,
+              int32_t *__restrict__ accepted_nodes, int32_t *__restrict__ commit_tokens,
+              int32_t *__restrict__ bonus, unsigned int *err) {
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x;
+    const int width = max_depth + 1;
+    const int base = qo_indptr[b];
+    const int T = qo_indptr[b + 1] - base;
+    int32_t *acc = accepted_nodes + (size_t)b * width;
+    int32_t *com = commit_tokens + (size_t)b * width;
+    if (T < 1 || T > DDT_MAX_Q_LEN) {
+        if (lane == 0) latch(err, DDT_DEVERR_QO_INDPTR);
+        return;
+    }
+    int cur = 0, n = 1;
+    int path[DDT_MAX_DEPTH + 1];  // lane 0 keeps the accepted nodes
+    path[0] = 0;
+    for (;;) {
+        const int want = target_argmax[base + cur];
+        int found = -1;
+        for (int c0 = 1; c0 < T && found < 0; c0 += 32) {
+            const int c = c0 + lane;
+            const bool hit = c < T && parent[base + c] == cur && node_token[base + c] == want;
+            const unsigned m = __ballot_sync(FULL, hit);
+            if (m) found = c0 + __ffs(m) - 1;
+        }
+        if (found < 0) break;
+        if (n >= width) {  // tree deeper than max_depth
+            if (lane == 0) latch(err, DDT_DEVERR_DEPTH);
+            break;
+        }
+        path[n] = found;
+        ++n;
+        cur = found;
+    }
+    const int bon = target_argmax[base + cur];
+    if (lane == 0) {
+        accept_len[b] = n;
+        bonus[b] = bon;
+    }
+    for (int k = lane; k < width; k += 32) {
+        acc[k] = (k < n) ? path[k] : -1;
+        int t = -1;
+        if (k < n - 1) t = node_token[base + path[k + 1]];
+        else if (k == n - 1) t = bon;
+        com[k] = t;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
+                              const int32_t *root_id, const int32_t *budget,
+                              const int32_t *qo_indptr, int batch, int max_depth, int topk,
+                              int32_t *node_token, int32_t *parent, int32_t *depth,
+                              unsigned int *err, cudaStream_t s) {
+    build_tree_kernel<<<batch, 32, 0, s>>>(topk_logp, topk_ids, root_id, budget, qo_indptr,
+                                           max_depth, topk, node_token, parent, depth, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
+                                      const int32_t *prefix_len, const int32_t *mask_indptr,
+                                      int batch, int total_words, uint32_t *mask,
+                                      unsigned int *err, cudaStream_t s) {
+    if (total_words <= 0) return cudaSuccess;
+    const int threads = 256;
+    int blocks = (total_words + threads - 1) / threads;
+    if (blocks > 4096) blocks = 4096;
+    compile_visibility_kernel<<<blocks, threads, 0, s>>>(parent, qo_indptr, prefix_len,
+                                                         mask_indptr, batch, total_words, mask,
+                                                         err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accept(const int32_t *node_token, const int32_t *parent,
+                          const int32_t *qo_indptr, const int32_t *target_argmax, int batch,
+                          int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
+                          int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
+                          cudaStream_t s) {
+    accept_kernel<<<batch, 32, 0, s>>>(node_token, parent, qo_indptr, target_argmax, max_depth,
+                                       accept_len, accepted_nodes, commit_tokens, bonus, err);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

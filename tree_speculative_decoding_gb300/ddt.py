@@ -1,0 +1,177 @@
+"""Thin ctypes binding of libddt.so (``include/ddt.h``).
+
+Argument marshalling only: torch tensors become device pointers, the current
+torch stream becomes the ``cudaStream_t``; every step of the verify path runs
+in the library's kernels.  There is no fallback: if the shared library is
+missing or fails to load, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+DL, DR, D = 512, 64, 576
+MAX_DEPTH, MAX_TOPK, MAX_Q_LEN, MAX_SPLITS = 7, 16, 128, 128
+
+STATUS = {0: "DDT_OK", 1: "DDT_ERR_INVALID_ARG", 2: "DDT_ERR_UNSUPPORTED", 3: "DDT_ERR_WORKSPACE",
+          4: "DDT_ERR_CUDA", 5: "DDT_ERR_DEVICE_CHECK", 6: "DDT_ERR_TIMEOUT"}
+
+
+class DDTError(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)}{(' ' + detail) if detail else ''}")
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libddt.so not built at {path}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    sig = {
+        "ddt_abi_version": ([], i32),
+        "ddt_status_string": ([i32], ctypes.c_char_p),
+        "ddt_build_tree": ([P, P, P, P, P, i32, i32, i32, P, P, P, P], i32),
+        "ddt_mask_indptr": ([P, P, i32, P], i32),
+        "ddt_compile_visibility": ([P, P, P, P, i32, i32, P, P], i32),
+        "ddt_verify_attn_num_splits": ([i32, i32, i32, i32, i32], i32),
+        "ddt_verify_attn_workspace_size": ([i32, i32, i32], sz),
+        "ddt_verify_attn": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P,
+                             sz, P], i32),
+        "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
+        "ddt_get_error": ([P, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, st):
+    if st != 0:
+        raise DDTError(fn, st)
+
+
+def _dev(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def abi_version() -> int:
+    return lib.ddt_abi_version()
+
+
+def ddt_build_tree(topk_logp, topk_ids, root_id, budget, qo_indptr, node_token, parent, depth,
+                   stream=None):
+    B, max_depth, K = topk_logp.shape
+    _dev(topk_logp, torch.float32, "topk_logp")
+    for n, t in (("topk_ids", topk_ids), ("root_id", root_id), ("budget", budget),
+                 ("qo_indptr", qo_indptr), ("node_token", node_token), ("parent", parent),
+                 ("depth", depth)):
+        _dev(t, torch.int32, n)
+    _check("ddt_build_tree", lib.ddt_build_tree(
+        _p(topk_logp), _p(topk_ids), _p(root_id), _p(budget), _p(qo_indptr), B, max_depth, K,
+        _p(node_token), _p(parent), _p(depth), _stream(stream)))
+
+
+def ddt_mask_indptr(qo_indptr_host, prefix_len_host):
+    """Host helper: int32 word offsets of the bit-packed mask (CPU tensors in/out)."""
+    qo = qo_indptr_host.to(torch.int32).contiguous().cpu()
+    pl = prefix_len_host.to(torch.int32).contiguous().cpu()
+    out = torch.empty(pl.numel() + 1, dtype=torch.int32)
+    _check("ddt_mask_indptr", lib.ddt_mask_indptr(_p(qo), _p(pl), pl.numel(), _p(out)))
+    return out
+
+
+def ddt_compile_visibility(parent, qo_indptr, prefix_len, mask_indptr, mask, stream=None):
+    for n, t in (("parent", parent), ("qo_indptr", qo_indptr), ("prefix_len", prefix_len),
+                 ("mask_indptr", mask_indptr)):
+        _dev(t, torch.int32, n)
+    if not (mask.is_cuda and mask.dtype in (torch.int32, torch.uint32) and mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous CUDA 32-bit tensor")
+    B = prefix_len.numel()
+    _check("ddt_compile_visibility", lib.ddt_compile_visibility(
+        _p(parent), _p(qo_indptr), _p(prefix_len), _p(mask_indptr), B, mask.numel(), _p(mask),
+        _stream(stream)))
+
+
+def ddt_verify_attn_num_splits(batch, num_heads, max_q_len, max_kv_len, num_sms=0):
+    return lib.ddt_verify_attn_num_splits(batch, num_heads, max_q_len, max_kv_len, num_sms)
+
+
+def ddt_verify_attn_workspace_size(total_q, num_heads, num_splits):
+    return lib.ddt_verify_attn_workspace_size(total_q, num_heads, num_splits)
+
+
+def ddt_verify_attn(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_indptr, scale,
+                    out, lse=None, max_q_len=None, max_kv_len=None, num_splits=0,
+                    workspace=None, stream=None):
+    """q: [total_q, H, 576] bf16; kv_pool: [pool_rows, 576] bf16; out: [total_q, H, 512] f32.
+
+    max_q_len / max_kv_len are host-side bounds used to size the grid; when
+    omitted they are read from the indptrs (a device->host copy)."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(kv_pool, torch.bfloat16, "kv_pool")
+    _dev(out, torch.float32, "out")
+    for n, t in (("kv_indices", kv_indices), ("kv_indptr", kv_indptr), ("qo_indptr", qo_indptr),
+                 ("mask_indptr", mask_indptr)):
+        _dev(t, torch.int32, n)
+    total_q, H, d = q.shape
+    if d != D or kv_pool.shape[-1] != D or tuple(out.shape) != (total_q, H, DL):
+        raise ValueError("q/kv_pool rows must be 576 wide and out [total_q, H, 512]")
+    B = qo_indptr.numel() - 1
+    if max_q_len is None or max_kv_len is None:
+        qo = qo_indptr.cpu()
+        kv = kv_indptr.cpu()
+        max_q_len = int((qo[1:] - qo[:-1]).max())
+        max_kv_len = int((kv[1:] - kv[:-1]).max())
+    if workspace is None:
+        splits = num_splits or ddt_verify_attn_num_splits(B, H, max_q_len, max_kv_len)
+        nbytes = ddt_verify_attn_workspace_size(total_q, H, splits)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device) if nbytes else None
+        num_splits = splits
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ddt_verify_attn", lib.ddt_verify_attn(
+        _p(q), _p(kv_pool), kv_pool.shape[0], _p(kv_indices), _p(kv_indptr), _p(qo_indptr),
+        _p(mask), _p(mask_indptr), B, H, total_q, int(max_q_len), int(max_kv_len), float(scale),
+        int(num_splits), _p(out), _p(lse), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def ddt_accept(node_token, parent, qo_indptr, target_argmax, max_depth, accept_len,
+               accepted_nodes, commit_tokens, bonus, stream=None):
+    for n, t in (("node_token", node_token), ("parent", parent), ("qo_indptr", qo_indptr),
+                 ("target_argmax", target_argmax), ("accept_len", accept_len),
+                 ("accepted_nodes", accepted_nodes), ("commit_tokens", commit_tokens),
+                 ("bonus", bonus)):
+        _dev(t, torch.int32, n)
+    B = qo_indptr.numel() - 1
+    _check("ddt_accept", lib.ddt_accept(
+        _p(node_token), _p(parent), _p(qo_indptr), _p(target_argmax), B, int(max_depth),
+        _p(accept_len), _p(accepted_nodes), _p(commit_tokens), _p(bonus), _stream(stream)))
+
+
+def ddt_get_error(stream=None):
+    """Returns (status, device_error_bits) and clears the device error word."""
+    word = ctypes.c_uint32(0)
+    st = lib.ddt_get_error(_stream(stream), ctypes.byref(word))
+    return st, word.value

@@ -1,0 +1,103 @@
+"""One DDTree verify step on the GPU through the C ABI.
+
+``VerifyStep`` owns the device buffers of one batch and runs the four stages
+in order on one stream: ddt_build_tree -> ddt_compile_visibility ->
+ddt_verify_attn -> ddt_accept (the per-iteration data flow of "The Oracle
+Drafter", section "The Engine Interface Design", with the mask and positions
+built on the device instead of the host).  It only allocates and calls the
+binding; all arithmetic runs in libddt.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import ddt
+
+
+def _i32(a, device):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def _bf16(a, device):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16).to(device)
+
+
+class VerifyStep:
+    """Device-resident inputs and outputs of one verify step for a Workload."""
+
+    def __init__(self, wl, device="cuda", target_argmax=None, num_splits=0):
+        self.wl = wl
+        self.device = torch.device(device)
+        dev = self.device
+        self.B, self.H = wl.B, wl.H
+        self.total_q = wl.total_q
+        self.max_q_len = int(wl.q_len.max())
+        self.max_kv_len = int(wl.kv_len.max())
+        self.topk_logp = torch.from_numpy(np.ascontiguousarray(wl.topk_logp)).to(dev)
+        self.topk_ids = _i32(wl.topk_ids, dev)
+        self.root_id = _i32(wl.root_id, dev)
+        self.budget = _i32(wl.budget, dev)
+        self.qo_indptr = _i32(wl.qo_indptr, dev)
+        self.kv_indptr = _i32(wl.kv_indptr, dev)
+        self.kv_indices = _i32(wl.kv_indices, dev)
+        self.prefix_len = _i32(wl.prefix_len, dev)
+        self.q = _bf16(wl.q, dev)
+        self.kv_pool = _bf16(wl.kv_pool, dev)
+        argmax = wl.argmax_random if target_argmax is None else target_argmax
+        self.target_argmax = _i32(argmax, dev)
+        mip = ddt.ddt_mask_indptr(torch.from_numpy(wl.qo_indptr.astype(np.int32)),
+                                  torch.from_numpy(wl.prefix_len.astype(np.int32)))
+        self.mask_indptr_host = mip
+        self.mask_indptr = mip.to(dev)
+        self.total_words = int(mip[-1])
+
+        T = self.total_q
+        self.node_token = torch.empty(T, dtype=torch.int32, device=dev)
+        self.parent = torch.empty(T, dtype=torch.int32, device=dev)
+        self.depth = torch.empty(T, dtype=torch.int32, device=dev)
+        self.mask = torch.empty(self.total_words, dtype=torch.int32, device=dev)
+        self.out = torch.empty((T, self.H, ddt.DL), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((T, self.H), dtype=torch.float32, device=dev)
+        W = wl.max_depth + 1
+        self.accept_len = torch.empty(self.B, dtype=torch.int32, device=dev)
+        self.accepted_nodes = torch.empty((self.B, W), dtype=torch.int32, device=dev)
+        self.commit_tokens = torch.empty((self.B, W), dtype=torch.int32, device=dev)
+        self.bonus = torch.empty(self.B, dtype=torch.int32, device=dev)
+
+        self.num_splits = num_splits or ddt.ddt_verify_attn_num_splits(
+            self.B, self.H, self.max_q_len, self.max_kv_len)
+        nbytes = ddt.ddt_verify_attn_workspace_size(T, self.H, self.num_splits)
+        self.workspace = (torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None)
+
+    # -- stages -------------------------------------------------------------
+    def build_tree(self, stream=None):
+        ddt.ddt_build_tree(self.topk_logp, self.topk_ids, self.root_id, self.budget,
+                           self.qo_indptr, self.node_token, self.parent, self.depth, stream)
+
+    def compile_visibility(self, stream=None):
+        ddt.ddt_compile_visibility(self.parent, self.qo_indptr, self.prefix_len, self.mask_indptr,
+                                   self.mask, stream)
+
+    def verify_attn(self, stream=None):
+        ddt.ddt_verify_attn(self.q, self.kv_pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
+                            self.mask, self.mask_indptr, self.wl.scale, self.out, self.lse,
+                            max_q_len=self.max_q_len, max_kv_len=self.max_kv_len,
+                            num_splits=self.num_splits, workspace=self.workspace, stream=stream)
+
+    def accept(self, stream=None):
+        ddt.ddt_accept(self.node_token, self.parent, self.qo_indptr, self.target_argmax,
+                       self.wl.max_depth, self.accept_len, self.accepted_nodes,
+                       self.commit_tokens, self.bonus, stream)
+
+    def run(self, stream=None):
+        self.build_tree(stream)
+        self.compile_visibility(stream)
+        self.verify_attn(stream)
+        self.accept(stream)
+
+    def check_device_errors(self):
+        st, bits = ddt.ddt_get_error()
+        if st != 0:
+            raise ddt.DDTError("device check", st, f"bits=0x{bits:x}")
