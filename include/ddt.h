@@ -191,6 +191,38 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
                            size_t workspace_bytes, void *stream);
 
 /*
+ * ddt_verify_attn_noalloc -- ddt_verify_attn without a caller workspace.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: an engine that reserved all device
+ * memory for its own pool up front, a plain C host without an allocator, or
+ * a decode loop in which a cudaMalloc (which may synchronise the whole
+ * device) is not allowed.  The call allocates nothing: when it splits the kv
+ * range, the split results live in a fixed array of
+ * DDT_NOALLOC_SCRATCH_BYTES inside libddt.so's device memory, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Arguments, outputs and errors are those of ddt_verify_attn minus the
+ * workspace.  If the chosen (or requested) split count needs more scratch
+ * than DDT_NOALLOC_SCRATCH_BYTES (see ddt_verify_attn_workspace_size), the
+ * call returns DDT_ERR_WORKSPACE and launches nothing; pass a smaller
+ * num_splits (1 needs no scratch) or use ddt_verify_attn.
+ * The first call on a device looks up the array's device address for that
+ * device; make that first call before any stream capture.  All calls share
+ * the one array: calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller.  Every scratch
+ * entry a call reads is written earlier in the same call, so nothing has to
+ * be cleared between calls.
+ */
+#define DDT_NOALLOC_SCRATCH_BYTES (32u << 20)
+ddt_status ddt_verify_attn_noalloc(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
+                                   const int32_t *kv_indices, const int32_t *kv_indptr,
+                                   const int32_t *qo_indptr, const uint32_t *mask,
+                                   const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
+                                   int32_t total_q, int32_t max_q_len, int32_t max_kv_len,
+                                   float scale, int32_t num_splits, float *out, float *lse,
+                                   void *stream);
+
+/*
  * ddt_accept -- greedy tree acceptance (follow_verified_tree).
  * Page: "The DDTree CUDA Graph Fix ..." section "The DDTree Architecture"
  * (walk from the root following the target's argmax into the matching child

@@ -248,3 +248,12 @@ ddt_status ddt_get_error(void *stream, uint32_t *device_error) {
 }
 
 }  // extern "C"
+
+namespace ddt {
+// Device address of the current device's error word (sets the device up on
+// first use, like every entry point); null on failure.
+unsigned int *device_error_word() {
+    DeviceState *st = device_state();
+    return st ? st->err : nullptr;
+}
+}  // namespace ddt

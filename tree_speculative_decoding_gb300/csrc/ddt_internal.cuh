@@ -67,4 +67,7 @@ int attn_kv_tile();
 // kernel attributes (dynamic shared memory opt-in).
 cudaError_t attn_prepare_device();
 
+// Device address of the current device's error word (null on failure).
+unsigned int *device_error_word();
+
 }  // namespace ddt

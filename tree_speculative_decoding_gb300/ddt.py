@@ -44,6 +44,8 @@ def _load():
         "ddt_verify_attn_workspace_size": ([i32, i32, i32], sz),
         "ddt_verify_attn": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P,
                              sz, P], i32),
+        "ddt_verify_attn_noalloc": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P,
+                                     P, P], i32),
         "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
         "ddt_get_error": ([P, P], i32),
     }
@@ -155,6 +157,35 @@ def ddt_verify_attn(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_ind
         _p(q), _p(kv_pool), kv_pool.shape[0], _p(kv_indices), _p(kv_indptr), _p(qo_indptr),
         _p(mask), _p(mask_indptr), B, H, total_q, int(max_q_len), int(max_kv_len), float(scale),
         int(num_splits), _p(out), _p(lse), _p(workspace), ws_bytes, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def ddt_verify_attn_noalloc(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_indptr,
+                            scale, out, lse=None, max_q_len=None, max_kv_len=None, num_splits=0,
+                            stream=None):
+    """ddt_verify_attn for callers that cannot allocate device memory (a
+    pre-reserved engine pool, a host without an allocator, a loop where a
+    device-synchronising cudaMalloc is not allowed): the split scratch is a
+    fixed 32 MiB array inside libddt.so, so neither this wrapper nor the call
+    allocates on the device.  Calls overlapping on the GPU race on that
+    array.  Raises DDTError(DDT_ERR_WORKSPACE) when the split count needs more
+    scratch than the array holds."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(kv_pool, torch.bfloat16, "kv_pool")
+    _dev(out, torch.float32, "out")
+    total_q, H, _ = q.shape
+    B = qo_indptr.numel() - 1
+    if max_q_len is None or max_kv_len is None:
+        qo = qo_indptr.cpu()
+        kv = kv_indptr.cpu()
+        max_q_len = int((qo[1:] - qo[:-1]).max())
+        max_kv_len = int((kv[1:] - kv[:-1]).max())
+    _check("ddt_verify_attn_noalloc", lib.ddt_verify_attn_noalloc(
+        _p(q), _p(kv_pool), kv_pool.shape[0], _p(kv_indices), _p(kv_indptr), _p(qo_indptr),
+        _p(mask), _p(mask_indptr), B, H, total_q, int(max_q_len), int(max_kv_len), float(scale),
+        int(num_splits), _p(out), _p(lse), _stream(stream)))
 
 
 def ddt_accept(node_token, parent, qo_indptr, target_argmax, max_depth, accept_len,
