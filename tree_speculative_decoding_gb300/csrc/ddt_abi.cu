@@ -53,15 +53,7 @@ inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
-    // CTAs without splitting: one per (request, node, 16-head group)
-    const long long ctas = (long long)batch * max_q_len * ((num_heads + 15) / 16);
-    const long long target = 2LL * num_sms;
-    long long splits = (target + ctas - 1) / ctas;
-    const long long by_len = max_kv_len / 256;  // keep >= 256 columns per split
-    if (splits > by_len) splits = by_len;
-    if (splits < 1) splits = 1;
-    if (splits > DDT_MAX_SPLITS) splits = DDT_MAX_SPLITS;
-    return (int)splits;
+    return ddt::attn_choose_splits(batch, num_heads, max_q_len, max_kv_len, num_sms);
 }
 
 }  // namespace

@@ -174,14 +174,12 @@ attn_simt_kernel(AttnArgs a) {
 
 }  // namespace
 
-int attn_kv_tile() { return kTile; }
-
-cudaError_t attn_prepare_device() {
+cudaError_t attn_simt_prepare_device() {
     return cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes);
 }
 
-cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
     const int hgroups = (a.num_heads + kHeads - 1) / kHeads;
     dim3 grid(a.num_splits, a.max_q_len * hgroups, a.batch);
     attn_simt_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);

@@ -1,0 +1,543 @@
+// ddt_attn_tc.cu -- tree-verify MLA attention on the sm_103a tensor cores.
+//
+// What it computes, per row (tree node i of request b, head h), over the kv
+// columns j of the request that mask row i makes visible:
+//   s_j = scale * <q[i,h,0:576], kv[idx_j, 0:576]>,
+//   out[i,h,:] = sum_j softmax(s)_j kv[idx_j, 0:512],  lse = log sum_j e^{s_j}
+// ("The Architecture of a Speculative Decoding Engine", section "The Forward
+// Pass Pseudocode": absorbed MLA, scores over latent + rope, output in the
+// latent space; "The 30-Column Mask", sections "The Message: Tensor Shapes as
+// Evidence" and "The Fix: Building Combined Indices": kv columns = prefix slots
+// then the tree nodes' slots, one 576-wide row per token shared by all heads).
+//
+// Tiling (GB300-specific, measured on the part):
+//   * A tile is 128 consecutive (node, head) rows of one request, e.g. two
+//     nodes x 64 heads.  A thread-block cluster of two CTAs owns one tile and
+//     one kv split.  CTA c keeps in tensor memory the fp32 output for latent
+//     half c (128 lanes x 256 columns) and its half of Q's 576 dims as bf16
+//     (latent [256c, 256c+256) and rope [512+32c, 512+32c+32): 144 columns);
+//     the rest holds the score block (96 columns).  A full-width output tile
+//     (512 columns) would leave no room for scores, which is why the latent
+//     dimension is split across the pair.
+//   * Per kv block of 96 columns: each CTA gathers its five 64-dim boxes of
+//     the 96 latent rows (four latent boxes + the rope box) with per-row TMA
+//     loads (128-byte swizzle), computes partial scores over its dim half
+//     (tcgen05.mma, A = Q from tensor memory, M=128, N=96), and the pair swaps
+//     fp32 partials through distributed shared memory: CTA c owns the softmax
+//     of rows [64c, 64c+64).  The owner adds the two partials, applies the
+//     mask, runs the online softmax (max rescale only when it grows by more
+//     than 2^8), and writes P (bf16) into both CTAs' shared memory with the
+//     row's rescale factor.  Each CTA then accumulates O_c += P V_c
+//     (tcgen05.mma, M=128, N=256, K=96, V read as an MN-major operand straight
+//     from the gathered boxes).
+//   * Warp roles: warps 0-3 softmax / epilogue (thread = row = TMEM lane),
+//     warp 4 TMA producer, warp 5 MMA issuer.  Two kv stages, two P buffers.
+//   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
+//     stops, and still meets its partner at the final cluster barrier.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "ddt_internal.cuh"
+#include "ddt_sm100.cuh"
+
+namespace ddt {
+namespace {
+
+using namespace sm100;
+
+constexpr int kRows = 128;            // rows per tile (TMEM lanes)
+constexpr int kNb = 96;               // kv columns per block
+constexpr int kThreads = 192;         // 6 warps
+constexpr int kBoxBytes = kNb * 128;  // 96 rows x 64 bf16
+constexpr int kBoxes = 5;             // 4 latent boxes of this CTA's half + rope box
+constexpr int kStageBytes = kBoxes * kBoxBytes;
+constexpr int kStages = 2;
+constexpr int kPBytes = 2 * kRows * 128;  // P: 128 rows x 96 kv bf16 in two 64-wide atoms
+constexpr int kXStride = 100;             // floats per row of the partner-partial buffer
+constexpr int kXBytes = 64 * kXStride * 4;
+
+constexpr int kOffStage = 0;
+constexpr int kOffP = kOffStage + kStages * kStageBytes;  // 122880
+constexpr int kOffX = kOffP + 2 * kPBytes;                // 188416
+constexpr int kOffAlpha = kOffX + kXBytes;                // 2 x 64 floats
+constexpr int kOffLinv = kOffAlpha + 2 * 64 * 4;          // 64 floats
+constexpr int kOffBar = kOffLinv + 64 * 4;
+// barrier slots
+enum {
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL, B_SFREE, B_XFULL, B_XEMPTY,
+    B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1, B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
+};
+constexpr int kOffHolder = kOffBar + B_COUNT * 8;
+constexpr int kOffAbort = kOffHolder + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+
+// tensor memory columns
+constexpr uint32_t kColO = 0;    // 256: output, latent half
+constexpr uint32_t kColQ = 256;  // 144: Q half (128 latent + 16 rope), bf16 pairs
+constexpr uint32_t kColS = 400;  // 96: partial scores
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr uint32_t kIdescS = idesc_bf16(kRows, kNb, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kColS + kNb <= kTmemCols, "tensor memory budget");
+
+struct TcParams {
+    AttnArgs a;
+    int tiles_per_req;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              unsigned int *err) {
+    if (*abort) return false;
+    if (mbar_wait(bar, parity, kWaitLimit)) return true;
+    *abort = 1;
+    latch(err, DDT_DEVERR_TIMEOUT);
+    return false;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUtensorMap kv_map) {
+    const AttnArgs &a = prm.a;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    uint32_t *holder = reinterpret_cast<uint32_t *>(smem + kOffHolder);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 or 1: latent half
+    const uint32_t peer = rank ^ 1u;
+    const int split = blockIdx.x >> 1;
+    const int tile = blockIdx.y;
+    const int b = blockIdx.z;
+
+    // ---- work of this tile / split (identical in both CTAs of the pair) ----
+    const int H = a.num_heads;
+    const int qo0 = a.qo_indptr[b];
+    const int T = a.qo_indptr[b + 1] - qo0;
+    const int kv0 = a.kv_indptr[b];
+    const int N = a.kv_indptr[b + 1] - kv0;
+    const int rows_req = T * H;
+    const int row0 = tile * kRows;
+    if (row0 >= rows_req) return;  // uniform in the pair: no cluster interaction yet
+    bool bad = false;
+    if (T > a.max_q_len || T < 1) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_QO_INDPTR); }
+    if (N < T || N > a.max_kv_len) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_KV_INDPTR); }
+    const int P = N - T;
+    const int W = (N + 31) >> 5;
+    if (!bad && a.mask_indptr[b + 1] - a.mask_indptr[b] != T * W) {
+        bad = true;
+        if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_MASK_INDPTR);
+    }
+    if (bad) return;  // uniform in the pair
+    const int rows_valid = min(kRows, rows_req - row0);
+    const int i_max = (row0 + rows_valid - 1) / H;   // last node in the tile
+    const int kv_end = P + i_max + 1;                 // nothing beyond is visible to the tile
+    const int c_begin = split * a.split_cols;
+    const int c_end = min(kv_end, c_begin + a.split_cols);
+    const int nblk = (c_end > c_begin) ? (c_end - c_begin + kNb - 1) / kNb : 0;
+    const int64_t rows_total = (int64_t)a.total_q * H;
+
+    if (nblk == 0) {  // empty split: neutral partial result (only happens with splits > 1)
+        if (warp < 4) {
+            const int r = tid;
+            if (r < rows_valid && a.num_splits > 1) {
+                const int rr = row0 + r;
+                const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
+                float *o = a.o_part + ((int64_t)split * rows_total + grow) * DDT_DL + 256 * rank;
+                for (int q = 0; q < 64; ++q) reinterpret_cast<float4 *>(o)[q] = make_float4(0, 0, 0, 0);
+                if (rank == 0) a.lse_part[(int64_t)split * rows_total + grow] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    // ---- setup ----
+    if (tid == 0) {
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 4, 2, 2, 2, 2, 2, 2, 4, 4, 1, 2};
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) tmem_alloc(smem_u32(holder), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    cluster_sync();  // both CTAs' barriers exist before any remote access
+
+    // softmax warps: this CTA's half of Q into tensor memory (thread = row = lane)
+    const int r = tid;  // row within the tile for warps 0-3
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    if (warp < 4) {
+        uint32_t w[32];
+        const bool valid = r < rows_valid;
+        const int rr = row0 + r;
+        const uint4 *src = nullptr;
+        if (valid) {
+            const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
+            src = reinterpret_cast<const uint4 *>(a.q + grow * DDT_D);
+        }
+        for (int part = 0; part < 4; ++part) {  // latent: 4 x 64 dims
+            for (int v = 0; v < 8; ++v) {
+                uint4 x = valid ? src[(256 * rank + 64 * part) / 8 + v] : make_uint4(0, 0, 0, 0);
+                w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+            }
+            tmem_st32(tmem + lane_off + kColQ + 32 * part, w);
+        }
+        for (int v = 0; v < 8; ++v) {  // rope half: 32 dims, then 16 zero columns
+            uint4 x = (valid && v < 4) ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+            w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_off + kColQ + 128, w);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == 4) {
+        // ================= TMA producer =================
+        for (int j = 0; j < nblk && !*abort_flag; ++j) {
+            const int s = j & 1, u = j >> 1;
+            if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL0 + s), kStageBytes);
+            const uint32_t stage = sbase + kOffStage + s * kStageBytes;
+            const int c0 = c_begin + j * kNb;
+            const int first_slot = a.kv_indices[kv0 + c_begin];
+            for (int k = lane; k < kNb; k += 32) {
+                const int c = c0 + k;
+                int slot = (c < c_end) ? a.kv_indices[kv0 + c] : first_slot;
+                if (slot < 0 || (int64_t)slot >= a.pool_rows) {
+                    latch(a.err, DDT_DEVERR_KV_INDEX);
+                    slot = 0;
+                }
+                const uint32_t dst = stage + k * 128;
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, &kv_map, 256 * rank + 64 * bx, slot,
+                                bar(B_FULL0 + s));
+                tma_load_2d(dst + 4 * kBoxBytes, &kv_map, 512, slot, bar(B_FULL0 + s));
+            }
+            __syncwarp();
+        }
+    } else if (warp == 5) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            auto issue_pv = [&](int k) -> bool {
+                const int s = k & 1;
+                if (!wait_or_abort(bar(B_PFULL0 + s), (k >> 1) & 1, abort_flag, a.err)) return false;
+                tc_fence_after();
+                const uint32_t pbuf = sbase + kOffP + s * kPBytes;
+                const uint32_t stage = sbase + kOffStage + s * kStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < kNb / 16; ++ks) {
+                    const uint64_t ad = smem_desc(pbuf + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(stage + ks * 2048, kBoxBytes, 1024);
+                    mma_ss(tmem + kColO, ad, bd, kIdescPV, (k > 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(B_EMPTY0 + s));
+                mma_commit_multicast(bar(B_PEMPTY0 + s), (uint16_t)0x3);
+                mma_commit(bar(B_PVDONE));
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                if (!wait_or_abort(bar(B_FULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                if (j > 0 && !wait_or_abort(bar(B_SFREE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t stage = sbase + kOffStage + s * kStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims
+                    const uint64_t bd = smem_desc(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
+                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims
+                    const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 64 * rank + 32 * ks, 16, 1024);
+                    mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * ks, bd, kIdescS, 1u);
+                }
+                mma_commit(bar(B_SFULL));
+                if (j > 0) ok = issue_pv(j - 1);
+            }
+            if (ok) issue_pv(nblk - 1);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax / epilogue (warps 0-3, thread = row) =================
+        const bool owner = (uint32_t)(warp >> 1) == rank;
+        const int xrow = r & 63;
+        const bool row_valid = r < rows_valid;
+        const int rr = row0 + r;
+        const int node = row_valid ? rr / H : 0;
+        const int head = row_valid ? rr % H : 0;
+        const uint32_t *mrow = a.mask + a.mask_indptr[b] + (int64_t)node * W;
+        const float sc = a.scale * kLog2e;
+        // cluster addresses of the partner's buffers / barriers
+        const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * (kXStride * 4), peer);
+        const uint32_t p_xfull = map_to_cta(bar(B_XFULL), peer);
+        const uint32_t p_xempty = map_to_cta(bar(B_XEMPTY), peer);
+        const uint32_t p_fin = map_to_cta(bar(B_FIN), peer);
+        const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < nblk && ok; ++j) {
+            const int s = j & 1;
+            // partial scores of this block from tensor memory
+            if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
+            tc_fence_after();
+            float sv[kNb];
+            {
+                uint32_t t32[32];
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SFREE));
+
+            if (!owner) {
+                // send this row's partial to its owner
+                if (j > 0 && !wait_or_abort(bar(B_XEMPTY), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+#pragma unroll
+                for (int q = 0; q < kNb / 4; ++q)
+                    st_async_v4(px_row + 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
+                                __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
+                // receive P rows (written into this CTA's P buffer) and the rescale factor
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
+                if (!wait_or_abort(bar(B_PIN0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                fence_proxy_async_smem();
+                const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
+                if (j > 0) {
+                    if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                        uint32_t t32[32];
+#pragma unroll 1
+                        for (int q = 0; q < 8; ++q) {
+                            tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
+                            tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_PFULL0 + s));
+            } else {
+                // owner: partner partial + own partial -> softmax -> P for both CTAs
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL), 32 * kNb * 4);
+                if (!wait_or_abort(bar(B_XFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
+                {
+                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + xrow * (kXStride * 4));
+#pragma unroll
+                    for (int q = 0; q < kNb / 4; ++q) {
+                        const float4 v = x[q];
+                        sv[4 * q] += v.x; sv[4 * q + 1] += v.y; sv[4 * q + 2] += v.z; sv[4 * q + 3] += v.w;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(p_xempty);
+                // mask: prefix columns are visible to every row; tree columns per mask bit
+                const int c0 = c_begin + j * kNb;
+                float mb = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kNb; ++k) {
+                    const int c = c0 + k;
+                    bool vis = row_valid && c < c_end;
+                    if (vis && c >= P) vis = (mrow[c >> 5] >> (c & 31)) & 1u;
+                    sv[k] = vis ? sv[k] * sc : -INFINITY;
+                    mb = fmaxf(mb, sv[k]);
+                }
+                float alpha = 1.0f;
+                if (mb > m_ref + 8.0f || (m_ref == -INFINITY && mb != -INFINITY)) {
+                    alpha = exp2f(m_ref - mb);  // 0 when nothing was seen before
+                    l *= alpha;
+                    m_ref = mb;
+                }
+                uint32_t pw[kNb / 2];
+                float lsum = 0.f;
+#pragma unroll
+                for (int k = 0; k < kNb; k += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (m_ref != -INFINITY) { p0 = exp2f(sv[k] - m_ref); p1 = exp2f(sv[k + 1] - m_ref); }
+                    lsum += p0 + p1;
+                    pw[k / 2] = pack_bf16(p0, p1);
+                }
+                l += lsum;
+                // both CTAs' P buffer s must be free (PV two blocks back done in both)
+                if (j >= 2 && !wait_or_abort(bar(B_PEMPTY0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                const uint32_t pbuf = kOffP + s * kPBytes;
+                const uint32_t p_pin = map_to_cta(bar(B_PIN0 + s), peer);
+#pragma unroll
+                for (int q = 0; q < 12; ++q) {  // 12 chunks of 8 kv, 128-byte swizzle
+                    const uint32_t off = pbuf + (q >> 3) * (kRows * 128) + (r >> 3) * 1024 +
+                                         (r & 7) * 128 + (((q & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(smem + off) =
+                        make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+                    st_async_v4(map_to_cta(sbase + off, peer), pw[4 * q], pw[4 * q + 1], pw[4 * q + 2],
+                                pw[4 * q + 3], p_pin);
+                }
+                st_async_b32(map_to_cta(sbase + kOffAlpha + (s * 64 + xrow) * 4, peer),
+                             __float_as_uint(j == 0 ? 1.0f : alpha), p_pin);
+                fence_proxy_async_smem();
+                if (j > 0) {
+                    if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                        uint32_t t32[32];
+#pragma unroll 1
+                        for (int q = 0; q < 8; ++q) {
+                            tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
+                            tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_PFULL0 + s));
+            }
+        }
+
+        // ---- epilogue: O_c / l into the output (or this split's partial) ----
+        if (ok && wait_or_abort(bar(B_PVDONE), (nblk - 1) & 1, abort_flag, a.err)) {
+            float linv = 0.f;
+            float lse_v = -INFINITY;
+            bool have = true;
+            if (owner) {
+                linv = (l > 0.f) ? 1.f / l : 0.f;
+                lse_v = (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                st_async_b32(p_linv, __float_as_uint(linv), p_fin);
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_FIN), 32 * 4);
+                have = wait_or_abort(bar(B_FIN), 0, abort_flag, a.err);
+                linv = reinterpret_cast<volatile float *>(smem + kOffLinv)[xrow];
+            }
+            tc_fence_after();
+            if (have) {
+                float *o = nullptr;
+                float *lp = nullptr;
+                if (row_valid) {
+                    const int64_t grow = (int64_t)(qo0 + node) * H + head;
+                    if (a.num_splits > 1) {
+                        o = a.o_part + ((int64_t)split * rows_total + grow) * DDT_DL;
+                        lp = a.lse_part + (int64_t)split * rows_total + grow;
+                    } else {
+                        o = a.out + grow * DDT_DL;
+                        lp = a.lse ? a.lse + grow : nullptr;
+                    }
+                    o += 256 * rank;
+                }
+                uint32_t t32[32];
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
+                    tmem_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            reinterpret_cast<float4 *>(o + 32 * q + e)[0] =
+                                make_float4(__uint_as_float(t32[e]) * linv, __uint_as_float(t32[e + 1]) * linv,
+                                            __uint_as_float(t32[e + 2]) * linv, __uint_as_float(t32[e + 3]) * linv);
+                    }
+                }
+                if (owner && row_valid && lp) *lp = lse_v;
+            }
+        }
+    }
+
+    // ---- teardown: nobody leaves while the partner may still write here ----
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
+
+cudaError_t attn_tc_prepare_device() {
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
+}
+
+int attn_kv_tile() { return kNb; }
+
+cudaError_t attn_prepare_device() {
+    cudaError_t e = attn_simt_prepare_device();
+    if (e != cudaSuccess) return e;
+    return attn_tc_prepare_device();
+}
+
+int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
+    const long long tiles = (long long)batch * (((long long)max_q_len * num_heads + kRows - 1) / kRows);
+    const long long pairs = num_sms / 2;
+    long long splits = pairs / tiles;
+    const long long by_len = max_kv_len / (4 * kNb);  // keep >= 4 blocks per split
+    if (splits > by_len) splits = by_len;
+    if (splits < 1) splits = 1;
+    if (splits > DDT_MAX_SPLITS) splits = DDT_MAX_SPLITS;
+    return (int)splits;
+}
+
+cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
+    if (!g_encode) return cudaErrorInitializationError;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)DDT_D, (cuuint64_t)a.pool_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)DDT_D * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult cr = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<uint16_t *>(a.kv_pool), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    TcParams prm;
+    prm.a = a;
+    prm.tiles_per_req = (a.max_q_len * a.num_heads + kRows - 1) / kRows;
+    dim3 grid(2 * a.num_splits, prm.tiles_per_req, a.batch);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(prm, map);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt
