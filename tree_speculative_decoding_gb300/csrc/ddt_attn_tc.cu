@@ -50,7 +50,7 @@ using namespace sm100;
 
 constexpr int kRows = 128;            // rows per tile (TMEM lanes)
 constexpr int kNb = 96;               // kv columns per block
-constexpr int kThreads = 192;         // 6 warps
+constexpr int kThreads = 224;         // 7 warps
 constexpr int kBoxBytes = kNb * 128;  // 96 rows x 64 bf16
 constexpr int kBoxes = 5;             // 4 latent boxes of this CTA's half + rope box
 constexpr int kStageBytes = kBoxes * kBoxBytes;
@@ -167,7 +167,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
     // ---- setup ----
     if (tid == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 4, 2, 2, 2, 2, 2, 2, 4, 4, 1, 2};
+        const uint32_t counts[B_COUNT] = {64, 64, 1, 1, 1, 4, 2, 2, 2, 2, 2, 2, 4, 4, 1, 2};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         *abort_flag = 0;
         fence_barrier_init();
@@ -209,37 +209,75 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
 
-    if (warp == 4) {
-        // ================= TMA producer =================
+    if (warp == 4 || warp == 6) {
+        // ================= producers: gather this CTA's five boxes per kv row =================
+        // Warp 4 moves kv rows [0, 48) of each block, warp 6 rows [48, 96).  One
+        // warp instruction moves one 128-byte box line of four kv rows: lane =
+        // 8 * (row within the group of four) + 16-byte chunk.  Chunks land with
+        // the 128-byte swizzle (chunk ^ (row & 7)) that the MMA descriptors
+        // expect.  Each lane arrives on the stage barrier once its own copies
+        // have landed (64 arrivals per stage).
+        const int half = (warp == 4) ? 0 : 1;
+        const int sub = lane >> 3, chunk = lane & 7;
+        const char *pool = reinterpret_cast<const char *>(a.kv_pool);
         for (int j = 0; j < nblk && !*abort_flag; ++j) {
             const int s = j & 1, u = j >> 1;
             if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL0 + s), kStageBytes);
             const uint32_t stage = sbase + kOffStage + s * kStageBytes;
-            const int c0 = c_begin + j * kNb;
-            const int first_slot = a.kv_indices[kv0 + c_begin];
-            for (int k = lane; k < kNb; k += 32) {
-                const int c = c0 + k;
-                int slot = (c < c_end) ? a.kv_indices[kv0 + c] : first_slot;
-                if (slot < 0 || (int64_t)slot >= a.pool_rows) {
-                    latch(a.err, DDT_DEVERR_KV_INDEX);
-                    slot = 0;
+            const int c0 = c_begin + j * kNb + 48 * half;
+            int slot_a, slot_b;  // slots of this warp's kv rows lane and lane + 32 (lane < 16)
+            {
+                int sl[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int c = min(c0 + lane + 32 * t, c_end - 1);  // rows past the end reuse a valid one
+                    int slot = a.kv_indices[kv0 + c];
+                    if (slot < 0 || (int64_t)slot >= a.pool_rows) {
+                        latch(a.err, DDT_DEVERR_KV_INDEX);
+                        slot = 0;
+                    }
+                    sl[t] = slot;
                 }
-                const uint32_t dst = stage + k * 128;
+                slot_a = sl[0]; slot_b = sl[1];
+            }
+#pragma unroll 4
+            for (int g = 0; g < 12; ++g) {
+                const int kk = 4 * g + sub;          // row within this warp's 48
+                const int k = 48 * half + kk;        // kv row within the block
+                const int mine = (g < 8) ? slot_a : slot_b;  // g < 8 <=> kk < 32, uniform
+                const int slot = __shfl_sync(0xffffffffu, mine, kk & 31);
+                const char *src = pool + (int64_t)slot * (DDT_D * 2) + chunk * 16;
+                const uint32_t dst = stage + (k >> 3) * 1024 + (k & 7) * 128 + ((chunk ^ (k & 7)) << 4);
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx)
-                    tma_load_2d(dst + bx * kBoxBytes, &kv_map, 256 * rank + 64 * bx, slot,
-                                bar(B_FULL0 + s));
-                tma_load_2d(dst + 4 * kBoxBytes, &kv_map, 512, slot, bar(B_FULL0 + s));
+                    cp_async_16(dst + bx * kBoxBytes, src + (256 * rank + 64 * bx) * 2);
+                cp_async_16(dst + 4 * kBoxBytes, src + 512 * 2);
             }
-            __syncwarp();
+            cp_async_arrive(bar(B_FULL0 + s));
         }
     } else if (warp == 5) {
         // ================= MMA issuer =================
+        // Issues S_j as soon as block j is loaded and the score buffer is free,
+        // and PV_j as soon as P_j is in place -- whichever is ready first.
         if (lane == 0) {
-            auto issue_pv = [&](int k) -> bool {
+            auto issue_s = [&](int j) {
+                const uint32_t stage = sbase + kOffStage + (j & 1) * kStageBytes;
+                fence_proxy_async_smem();  // stage written by cp.async, read by the tensor core
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims
+                    const uint64_t bd = smem_desc(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
+                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims
+                    const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 64 * rank + 32 * ks, 16, 1024);
+                    mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * ks, bd, kIdescS, 1u);
+                }
+                mma_commit(bar(B_SFULL));
+            };
+            auto issue_pv = [&](int k) {
                 const int s = k & 1;
-                if (!wait_or_abort(bar(B_PFULL0 + s), (k >> 1) & 1, abort_flag, a.err)) return false;
                 tc_fence_after();
                 const uint32_t pbuf = sbase + kOffP + s * kPBytes;
                 const uint32_t stage = sbase + kOffStage + s * kStageBytes;
@@ -252,29 +290,29 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 mma_commit(bar(B_EMPTY0 + s));
                 mma_commit_multicast(bar(B_PEMPTY0 + s), (uint16_t)0x3);
                 mma_commit(bar(B_PVDONE));
-                return true;
             };
-            bool ok = true;
-            for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
-                if (!wait_or_abort(bar(B_FULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                if (j > 0 && !wait_or_abort(bar(B_SFREE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t stage = sbase + kOffStage + s * kStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims
-                    const uint64_t bd = smem_desc(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, ks > 0 ? 1u : 0u);
+            int ns = 0, np = 0;  // next S block, next PV block
+            uint32_t idle = 0;
+            while (np < nblk) {
+                if (*abort_flag) break;
+                bool did = false;
+                if (ns < nblk && mbar_try_wait(bar(B_FULL0 + (ns & 1)), (ns >> 1) & 1) &&
+                    (ns == 0 || mbar_try_wait(bar(B_SFREE), (ns - 1) & 1))) {
+                    issue_s(ns++);
+                    did = true;
                 }
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims
-                    const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 64 * rank + 32 * ks, 16, 1024);
-                    mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * ks, bd, kIdescS, 1u);
+                if (np < ns && mbar_try_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)) {
+                    issue_pv(np++);
+                    did = true;
                 }
-                mma_commit(bar(B_SFULL));
-                if (j > 0) ok = issue_pv(j - 1);
+                if (did) {
+                    idle = 0;
+                } else if (++idle > kWaitLimit) {
+                    *abort_flag = 1;
+                    latch(a.err, DDT_DEVERR_TIMEOUT);
+                    break;
+                }
             }
-            if (ok) issue_pv(nblk - 1);
         }
         __syncwarp();
     } else {
@@ -296,58 +334,76 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < nblk && ok; ++j) {
-            const int s = j & 1;
-            // partial scores of this block from tensor memory
-            if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
+        // read S_j into registers and hand the score buffer back to the MMA warp
+        auto load_scores = [&](int j, float (&sv)[kNb]) -> bool {
+            if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) return false;
             tc_fence_after();
-            float sv[kNb];
-            {
-                uint32_t t32[32];
+            uint32_t t32[32];
 #pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
-                    tmem_wait_ld();
+            for (int q = 0; q < 3; ++q) {
+                tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
-                }
+                for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_SFREE));
+            return true;
+        };
+        // O row *= alpha once PV_{j-1} is done (needed by both roles before P_j is used)
+        auto finish_block = [&](int j, float alpha) -> bool {
+            if (j > 0) {
+                if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) return false;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    uint32_t t32[32];
+#pragma unroll 1
+                    for (int q = 0; q < 8; ++q) {
+                        tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
+                        tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PFULL0 + (j & 1)));
+            return true;
+        };
 
-            if (!owner) {
-                // send this row's partial to its owner
-                if (j > 0 && !wait_or_abort(bar(B_XEMPTY), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+        if (!owner) {
+            // Rows owned by the partner: send each block's partial scores as soon as
+            // they exist (one block ahead of the P this warp is waiting for), then
+            // take the partner's P rows and rescale factor for the block before.
+            auto send_partial = [&](int j) -> bool {
+                float sv[kNb];
+                if (!load_scores(j, sv)) return false;
+                if (j > 0 && !wait_or_abort(bar(B_XEMPTY), (j - 1) & 1, abort_flag, a.err)) return false;
 #pragma unroll
                 for (int q = 0; q < kNb / 4; ++q)
                     st_async_v4(px_row + 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
                                 __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
-                // receive P rows (written into this CTA's P buffer) and the rescale factor
+                return true;
+            };
+            ok = send_partial(0);
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                if (j + 1 < nblk && !send_partial(j + 1)) { ok = false; break; }
                 if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
                 if (!wait_or_abort(bar(B_PIN0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();  // P rows written by the partner, read by the tensor core
                 const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
-                if (j > 0) {
-                    if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-                        uint32_t t32[32];
-#pragma unroll 1
-                        for (int q = 0; q < 8; ++q) {
-                            tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
-                            tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_PFULL0 + s));
-            } else {
+                if (!finish_block(j, alpha)) { ok = false; break; }
+            }
+        } else {
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                float sv[kNb];
+                if (!load_scores(j, sv)) { ok = false; break; }
                 // owner: partner partial + own partial -> softmax -> P for both CTAs
                 if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL), 32 * kNb * 4);
                 if (!wait_or_abort(bar(B_XFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
@@ -361,29 +417,46 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(p_xempty);
-                // mask: prefix columns are visible to every row; tree columns per mask bit
+                // mask: prefix columns are visible to every row; only blocks reaching
+                // the tree columns (at most two per split) read mask words
                 const int c0 = c_begin + j * kNb;
                 float mb = -INFINITY;
+                if (row_valid && c0 + kNb <= min(P, c_end)) {
 #pragma unroll
-                for (int k = 0; k < kNb; ++k) {
-                    const int c = c0 + k;
-                    bool vis = row_valid && c < c_end;
-                    if (vis && c >= P) vis = (mrow[c >> 5] >> (c & 31)) & 1u;
-                    sv[k] = vis ? sv[k] * sc : -INFINITY;
-                    mb = fmaxf(mb, sv[k]);
+                    for (int k = 0; k < kNb; ++k) {
+                        sv[k] *= sc;
+                        mb = fmaxf(mb, sv[k]);
+                    }
+                } else {
+                    uint32_t mw[4] = {0u, 0u, 0u, 0u};  // words covering columns [32*(c0/32), +128)
+                    const int w0 = c0 >> 5;
+                    if (row_valid) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            if (w0 + t < W) mw[t] = mrow[w0 + t];
+                    }
+#pragma unroll
+                    for (int k = 0; k < kNb; ++k) {
+                        const int c = c0 + k;
+                        const int rel = c - 32 * w0;  // 0 .. 126
+                        const uint32_t word = rel < 32 ? mw[0] : (rel < 64 ? mw[1] : (rel < 96 ? mw[2] : mw[3]));
+                        const bool vis = row_valid && c < c_end && (c < P || ((word >> (rel & 31)) & 1u));
+                        sv[k] = vis ? sv[k] * sc : -INFINITY;
+                        mb = fmaxf(mb, sv[k]);
+                    }
                 }
                 float alpha = 1.0f;
-                if (mb > m_ref + 8.0f || (m_ref == -INFINITY && mb != -INFINITY)) {
-                    alpha = exp2f(m_ref - mb);  // 0 when nothing was seen before
+                if (mb > m_ref + 8.0f) {  // also true for the first visible block (m_ref = -inf)
+                    alpha = ex2(m_ref - mb);  // 0 when nothing was seen before
                     l *= alpha;
                     m_ref = mb;
                 }
                 uint32_t pw[kNb / 2];
                 float lsum = 0.f;
+                const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;  // all -inf rows give p = 0
 #pragma unroll
                 for (int k = 0; k < kNb; k += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (m_ref != -INFINITY) { p0 = exp2f(sv[k] - m_ref); p1 = exp2f(sv[k + 1] - m_ref); }
+                    const float p0 = ex2(sv[k] - mref), p1 = ex2(sv[k + 1] - mref);
                     lsum += p0 + p1;
                     pw[k / 2] = pack_bf16(p0, p1);
                 }
@@ -403,26 +476,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 }
                 st_async_b32(map_to_cta(sbase + kOffAlpha + (s * 64 + xrow) * 4, peer),
                              __float_as_uint(j == 0 ? 1.0f : alpha), p_pin);
-                fence_proxy_async_smem();
-                if (j > 0) {
-                    if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-                        uint32_t t32[32];
-#pragma unroll 1
-                        for (int q = 0; q < 8; ++q) {
-                            tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
-                            tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_PFULL0 + s));
+                fence_proxy_async_smem();  // local P rows, read by the tensor core
+                if (!finish_block(j, alpha)) { ok = false; break; }
             }
         }
 

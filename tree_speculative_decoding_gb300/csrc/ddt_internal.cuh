@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ddt.h"
+#include "ddt.h"
 
 namespace ddt {
 

@@ -114,6 +114,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy through L2 only (no L1 allocation)
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes this arrival)
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets, descriptor version 1, layout (2 = 128-byte swizzle).
@@ -201,6 +212,13 @@ __device__ __forceinline__ void tmem_wait_ld() {
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (flush-to-zero; exact 0 for -inf)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
