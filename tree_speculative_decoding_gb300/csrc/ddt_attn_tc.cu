@@ -70,7 +70,8 @@ enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL, B_SFREE, B_XFULL, B_XEMPTY,
     B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1, B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
 };
-constexpr int kOffHolder = kOffBar + B_COUNT * 8;
+constexpr int kOffXsig = kOffBar + B_COUNT * 8;   // 8-byte landing slot of the x_empty signal
+constexpr int kOffHolder = kOffXsig + 8;
 constexpr int kOffAbort = kOffHolder + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -329,6 +330,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * (kXStride * 4), peer);
         const uint32_t p_xfull = map_to_cta(bar(B_XFULL), peer);
         const uint32_t p_xempty = map_to_cta(bar(B_XEMPTY), peer);
+        const uint32_t p_xsig = map_to_cta(sbase + kOffXsig + 4 * (warp & 1), peer);
+        const uint32_t peer_base = map_to_cta(sbase, peer);
         const uint32_t p_fin = map_to_cta(bar(B_FIN), peer);
         const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
         float m_ref = -INFINITY, l = 0.f;
@@ -377,27 +380,70 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
         if (!owner) {
             // Rows owned by the partner: send each block's partial scores as soon as
-            // they exist (one block ahead of the P this warp is waiting for), then
-            // take the partner's P rows and rescale factor for the block before.
-            auto send_partial = [&](int j) -> bool {
-                float sv[kNb];
-                if (!load_scores(j, sv)) return false;
-                if (j > 0 && !wait_or_abort(bar(B_XEMPTY), (j - 1) & 1, abort_flag, a.err)) return false;
+            // they exist and take the partner's P rows (and rescale factor) as soon
+            // as they land -- whichever is ready first; at most one send ahead.
+            int nsend = 0, nfin = 0;
+            bool pin_armed = false;
+            uint32_t idle = 0;
+            while (nfin < nblk && ok) {
+                if (*abort_flag) { ok = false; break; }
+                bool did = false;
+                // uniform readiness tests (tcgen05.ld below is warp-collective)
+                bool can_send = false;
+                if (nsend < nblk && nsend <= nfin + 1) {
+                    bool t = mbar_try_wait(bar(B_SFULL), nsend & 1) &&
+                             (nsend == 0 || mbar_try_wait(bar(B_XEMPTY), (nsend - 1) & 1));
+                    can_send = __shfl_sync(0xffffffffu, t, 0);
+                }
+                if (can_send) {
+                    const int j = nsend++;
+                    float sv[kNb];
+                    tc_fence_after();
+                    {
+                        uint32_t t32[32];
 #pragma unroll
-                for (int q = 0; q < kNb / 4; ++q)
-                    st_async_v4(px_row + 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
-                                __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
-                return true;
-            };
-            ok = send_partial(0);
-            for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
-                if (j + 1 < nblk && !send_partial(j + 1)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
-                if (!wait_or_abort(bar(B_PIN0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                fence_proxy_async_smem();  // P rows written by the partner, read by the tensor core
-                const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
-                if (!finish_block(j, alpha)) { ok = false; break; }
+                        for (int q = 0; q < 3; ++q) {
+                            tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_SFREE));
+#pragma unroll
+                    for (int q = 0; q < kNb / 4; ++q)
+                        st_async_v4(px_row + 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
+                                    __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
+                    // the owner signals "read" with a 4-byte store per owner warp
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY), 4);
+                    (void)j;
+                    did = true;
+                }
+                if (nfin < nsend) {
+                    const int s = nfin & 1;
+                    if (!pin_armed) {
+                        if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
+                        pin_armed = true;
+                    }
+                    const bool t = __shfl_sync(0xffffffffu, mbar_try_wait(bar(B_PIN0 + s), (nfin >> 1) & 1), 0);
+                    if (t) {
+                        fence_proxy_async_smem();  // P rows written by the partner, read by the tensor core
+                        const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
+                        if (!finish_block(nfin, alpha)) { ok = false; break; }
+                        ++nfin;
+                        pin_armed = false;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle = 0;
+                } else if (++idle > kWaitLimit) {
+                    *abort_flag = 1;
+                    latch(a.err, DDT_DEVERR_TIMEOUT);
+                    ok = false;
+                }
             }
         } else {
             for (int j = 0; j < nblk && ok; ++j) {
@@ -416,7 +462,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(p_xempty);
+                if (lane == 0) st_async_b32(p_xsig, 0u, p_xempty);
                 // mask: prefix columns are visible to every row; only blocks reaching
                 // the tree columns (at most two per split) read mask words
                 const int c0 = c_begin + j * kNb;
@@ -471,10 +517,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                                          (r & 7) * 128 + (((q & 7) ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(smem + off) =
                         make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-                    st_async_v4(map_to_cta(sbase + off, peer), pw[4 * q], pw[4 * q + 1], pw[4 * q + 2],
+                    st_async_v4(peer_base + off, pw[4 * q], pw[4 * q + 1], pw[4 * q + 2],
                                 pw[4 * q + 3], p_pin);
                 }
-                st_async_b32(map_to_cta(sbase + kOffAlpha + (s * 64 + xrow) * 4, peer),
+                st_async_b32(peer_base + kOffAlpha + (s * 64 + xrow) * 4,
                              __float_as_uint(j == 0 ? 1.0f : alpha), p_pin);
                 fence_proxy_async_smem();  // local P rows, read by the tensor core
                 if (!finish_block(j, alpha)) { ok = false; break; }
