@@ -19,19 +19,23 @@
 //     the rest holds the score block (96 columns).  A full-width output tile
 //     (512 columns) would leave no room for scores, which is why the latent
 //     dimension is split across the pair.
-//   * Per kv block of 96 columns: each CTA gathers its five 64-dim boxes of
-//     the 96 latent rows (four latent boxes + the rope box) with per-row TMA
-//     loads (128-byte swizzle), computes partial scores over its dim half
-//     (tcgen05.mma, A = Q from tensor memory, M=128, N=96), and the pair swaps
-//     fp32 partials through distributed shared memory: CTA c owns the softmax
-//     of rows [64c, 64c+64).  The owner adds the two partials, applies the
-//     mask, runs the online softmax (max rescale only when it grows by more
-//     than 2^8), and writes P (bf16) into both CTAs' shared memory with the
-//     row's rescale factor.  Each CTA then accumulates O_c += P V_c
-//     (tcgen05.mma, M=128, N=256, K=96, V read as an MN-major operand straight
-//     from the gathered boxes).
+//   * Per kv block of 96 columns: two producer warps gather this CTA's half of
+//     the 96 kv rows with 16-byte cp.async copies into a 128-byte-swizzled
+//     stage (three stages); the MMA warp computes partial scores over the dim
+//     half (tcgen05.mma, A = Q from tensor memory, M=128, N=96).  The pair
+//     swaps fp32 partials through distributed shared memory: CTA c owns the
+//     softmax of rows [64c, 64c+64).  The owner adds the two partials, applies
+//     the mask, runs the online softmax (max rescale only when it grows by
+//     more than 2^8), writes P (bf16) locally and bulk-copies its rows to the
+//     partner with the rows' rescale factors.  Each CTA then accumulates
+//     O_c += P V_c (tcgen05.mma, M=128, N=256, K=96, V read as an MN-major
+//     operand straight from the gathered stage).
+//   * Distributed-shared-memory traffic moves at ~20 B/clk per direction only
+//     when a warp's stores cover contiguous 512-byte runs (scattered 16-byte
+//     pieces measured 8-9 B/clk), hence the chunk-major partial buffer and the
+//     bulk-copied P rows.
 //   * Warp roles: warps 0-3 softmax / epilogue (thread = row = TMEM lane),
-//     warp 4 TMA producer, warp 5 MMA issuer.  Two kv stages, two P buffers.
+//     warps 4 and 6 producers, warp 5 MMA issuer.
 //   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
 //     stops, and still meets its partner at the final cluster barrier.
 #include <cuda.h>
@@ -51,24 +55,29 @@ using namespace sm100;
 constexpr int kRows = 128;            // rows per tile (TMEM lanes)
 constexpr int kNb = 96;               // kv columns per block
 constexpr int kThreads = 224;         // 7 warps
-constexpr int kBoxBytes = kNb * 128;  // 96 rows x 64 bf16
-constexpr int kBoxes = 5;             // 4 latent boxes of this CTA's half + rope box
-constexpr int kStageBytes = kBoxes * kBoxBytes;
-constexpr int kStages = 2;
-constexpr int kPBytes = 2 * kRows * 128;  // P: 128 rows x 96 kv bf16 in two 64-wide atoms
-constexpr int kXStride = 100;             // floats per row of the partner-partial buffer
-constexpr int kXBytes = 64 * kXStride * 4;
+constexpr int kBoxBytes = kNb * 128;  // 96 rows x 64 bf16, 128-byte swizzle
+constexpr int kRopeBytes = kNb * 64;  // 96 rows x this CTA's 32 rope dims, 64-byte swizzle
+constexpr int kStageBytes = 4 * kBoxBytes + kRopeBytes;  // 4 latent boxes + rope half
+constexpr int kStages = 3;
+// P (128 rows x 96 kv, bf16): kv 0-63 in a 128-byte-swizzle atom column, kv
+// 64-95 in a 64-byte-swizzle one, so the 32 rows of one warp are contiguous in
+// each (4 KB + 2 KB) and go to the partner as two bulk copies.
+constexpr int kP0Bytes = kRows * 128;
+constexpr int kPBytes = kP0Bytes + kRows * 64;
+// partner partial scores: [24 chunks of 4 columns][64 rows] x 16 bytes, so one
+// warp's 16-byte stores for a chunk are 512 contiguous bytes
+constexpr int kXBytes = (kNb / 4) * 64 * 16;
 
 constexpr int kOffStage = 0;
-constexpr int kOffP = kOffStage + kStages * kStageBytes;  // 122880
-constexpr int kOffX = kOffP + 2 * kPBytes;                // 188416
+constexpr int kOffP = kOffStage + kStages * kStageBytes;
+constexpr int kOffX = kOffP + kPBytes;                    // one P buffer
 constexpr int kOffAlpha = kOffX + kXBytes;                // 2 x 64 floats
 constexpr int kOffLinv = kOffAlpha + 2 * 64 * 4;          // 64 floats
 constexpr int kOffBar = kOffLinv + 64 * 4;
 // barrier slots
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL, B_SFREE, B_XFULL, B_XEMPTY,
-    B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1, B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
+    B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_SFULL, B_SFREE, B_XFULL,
+    B_XEMPTY, B_PIN0, B_PIN1, B_PEMPTY, B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
 };
 constexpr int kOffXsig = kOffBar + B_COUNT * 8;   // 8-byte landing slot of the x_empty signal
 constexpr int kOffHolder = kOffXsig + 8;
@@ -168,7 +177,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
     // ---- setup ----
     if (tid == 0) {
-        const uint32_t counts[B_COUNT] = {64, 64, 1, 1, 1, 4, 2, 2, 2, 2, 2, 2, 4, 4, 1, 2};
+        const uint32_t counts[B_COUNT] = {64, 64, 64, 1, 1, 1, 1, 4, 2, 2, 2, 2, 2, 4, 4, 1, 2};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         *abort_flag = 0;
         fence_barrier_init();
@@ -183,6 +192,17 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
     // softmax warps: this CTA's half of Q into tensor memory (thread = row = lane)
     const int r = tid;  // row within the tile for warps 0-3
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Every MMA accumulates (enable-input-D set): an MMA that overwrites its
+    // accumulator right behind a tcgen05.commit waits for the committed MMAs to
+    // drain, which measured ~700-950 cycles per score block on the part.  The
+    // score columns are therefore cleared by the warps that read them, and O
+    // once at the start.
+    auto zero_scores = [&]() {
+        const uint32_t z[32] = {};
+#pragma unroll
+        for (int q = 0; q < 3; ++q) tmem_st32(tmem + lane_off + kColS + 32 * q, z);
+        tmem_wait_st();
+    };
     if (warp < 4) {
         uint32_t w[32];
         const bool valid = r < rows_valid;
@@ -204,11 +224,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
             w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
         }
         tmem_st32(tmem + lane_off + kColQ + 128, w);
-        tmem_wait_st();
+        const uint32_t z[32] = {};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tmem_st32(tmem + lane_off + kColO + 32 * q, z);
+        zero_scores();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    // Q / O / S in tensor memory before the first MMA: the softmax warps and the
+    // MMA warp meet on a named barrier; the producers start gathering at once.
+    if (warp < 4 || warp == 5) {
+        tc_fence_before();
+        named_barrier(1, 160);
+        tc_fence_after();
+    }
 
     if (warp == 4 || warp == 6) {
         // ================= producers: gather this CTA's five boxes per kv row =================
@@ -221,26 +248,33 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         const int half = (warp == 4) ? 0 : 1;
         const int sub = lane >> 3, chunk = lane & 7;
         const char *pool = reinterpret_cast<const char *>(a.kv_pool);
+        // slots of this warp's kv rows lane and lane + 32 (lane < 16) of block j;
+        // loaded one block ahead so the index fetch overlaps the wait for a free stage
+        auto fetch_slots = [&](int j, int (&sl)[2]) {
+            const int c0 = c_begin + j * kNb + 48 * half;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                sl[t] = a.kv_indices[kv0 + min(c0 + lane + 32 * t, c_end - 1)];  // rows past the end reuse a valid one
+        };
+        int next_sl[2];
+        fetch_slots(0, next_sl);
         for (int j = 0; j < nblk && !*abort_flag; ++j) {
-            const int s = j & 1, u = j >> 1;
+            const int s = j % kStages, u = j / kStages;
             if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) break;
             const uint32_t stage = sbase + kOffStage + s * kStageBytes;
-            const int c0 = c_begin + j * kNb + 48 * half;
-            int slot_a, slot_b;  // slots of this warp's kv rows lane and lane + 32 (lane < 16)
+            int slot_a, slot_b;
             {
-                int sl[2];
+                int sl[2] = {next_sl[0], next_sl[1]};
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    const int c = min(c0 + lane + 32 * t, c_end - 1);  // rows past the end reuse a valid one
-                    int slot = a.kv_indices[kv0 + c];
-                    if (slot < 0 || (int64_t)slot >= a.pool_rows) {
+                    if (sl[t] < 0 || (int64_t)sl[t] >= a.pool_rows) {
                         latch(a.err, DDT_DEVERR_KV_INDEX);
-                        slot = 0;
+                        sl[t] = 0;
                     }
-                    sl[t] = slot;
                 }
                 slot_a = sl[0]; slot_b = sl[1];
             }
+            if (j + 1 < nblk) fetch_slots(j + 1, next_sl);
 #pragma unroll 4
             for (int g = 0; g < 12; ++g) {
                 const int kk = 4 * g + sub;          // row within this warp's 48
@@ -252,7 +286,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx)
                     cp_async_16(dst + bx * kBoxBytes, src + (256 * rank + 64 * bx) * 2);
-                cp_async_16(dst + 4 * kBoxBytes, src + 512 * 2);
+                if (chunk < 4)  // rope: this CTA's 32 dims, 64-byte rows
+                    cp_async_16(stage + 4 * kBoxBytes + k * 64 + ((chunk ^ ((k >> 1) & 3)) << 4),
+                                src + (512 + 32 * rank) * 2);
             }
             cp_async_arrive(bar(B_FULL0 + s));
         }
@@ -262,34 +298,35 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         // and PV_j as soon as P_j is in place -- whichever is ready first.
         if (lane == 0) {
             auto issue_s = [&](int j) {
-                const uint32_t stage = sbase + kOffStage + (j & 1) * kStageBytes;
+                const uint32_t stage = sbase + kOffStage + (j % kStages) * kStageBytes;
                 fence_proxy_async_smem();  // stage written by cp.async, read by the tensor core
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims
                     const uint64_t bd = smem_desc(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, ks > 0 ? 1u : 0u);
+                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, 1u);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims
-                    const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 64 * rank + 32 * ks, 16, 1024);
+                    const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 32 * ks, 16, 512, kSwizzle64B);
                     mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * ks, bd, kIdescS, 1u);
                 }
                 mma_commit(bar(B_SFULL));
             };
             auto issue_pv = [&](int k) {
-                const int s = k & 1;
+                const int s = k % kStages;
                 tc_fence_after();
-                const uint32_t pbuf = sbase + kOffP + s * kPBytes;
+                const uint32_t pbuf = sbase + kOffP;
                 const uint32_t stage = sbase + kOffStage + s * kStageBytes;
 #pragma unroll
                 for (int ks = 0; ks < kNb / 16; ++ks) {
-                    const uint64_t ad = smem_desc(pbuf + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t ad = (ks < 4) ? smem_desc(pbuf + ks * 32, 16, 1024)
+                                                 : smem_desc(pbuf + kP0Bytes + (ks - 4) * 32, 16, 512, kSwizzle64B);
                     const uint64_t bd = smem_desc(stage + ks * 2048, kBoxBytes, 1024);
-                    mma_ss(tmem + kColO, ad, bd, kIdescPV, (k > 0 || ks > 0) ? 1u : 0u);
+                    mma_ss(tmem + kColO, ad, bd, kIdescPV, 1u);
                 }
                 mma_commit(bar(B_EMPTY0 + s));
-                mma_commit_multicast(bar(B_PEMPTY0 + s), (uint16_t)0x3);
+                mma_commit_multicast(bar(B_PEMPTY), (uint16_t)0x3);
                 mma_commit(bar(B_PVDONE));
             };
             int ns = 0, np = 0;  // next S block, next PV block
@@ -297,7 +334,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
             while (np < nblk) {
                 if (*abort_flag) break;
                 bool did = false;
-                if (ns < nblk && mbar_try_wait(bar(B_FULL0 + (ns & 1)), (ns >> 1) & 1) &&
+                if (ns < nblk && mbar_try_wait(bar(B_FULL0 + ns % kStages), (ns / kStages) & 1) &&
                     (ns == 0 || mbar_try_wait(bar(B_SFREE), (ns - 1) & 1))) {
                     issue_s(ns++);
                     did = true;
@@ -327,7 +364,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         const uint32_t *mrow = a.mask + a.mask_indptr[b] + (int64_t)node * W;
         const float sc = a.scale * kLog2e;
         // cluster addresses of the partner's buffers / barriers
-        const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * (kXStride * 4), peer);
+        const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * 16, peer);
         const uint32_t p_xfull = map_to_cta(bar(B_XFULL), peer);
         const uint32_t p_xempty = map_to_cta(bar(B_XEMPTY), peer);
         const uint32_t p_xsig = map_to_cta(sbase + kOffXsig + 4 * (warp & 1), peer);
@@ -349,6 +386,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
             }
+            zero_scores();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_SFREE));
@@ -409,12 +447,13 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                             for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
                         }
                     }
+                    zero_scores();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_SFREE));
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q)
-                        st_async_v4(px_row + 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
+                        st_async_v4(px_row + 64 * 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
                                     __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
                     // the owner signals "read" with a 4-byte store per owner warp
                     if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY), 4);
@@ -454,43 +493,49 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL), 32 * kNb * 4);
                 if (!wait_or_abort(bar(B_XFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
                 {
-                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + xrow * (kXStride * 4));
+                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX) + xrow;
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q) {
-                        const float4 v = x[q];
+                        const float4 v = x[64 * q];
                         sv[4 * q] += v.x; sv[4 * q + 1] += v.y; sv[4 * q + 2] += v.z; sv[4 * q + 3] += v.w;
                     }
                 }
                 __syncwarp();
                 if (lane == 0) st_async_b32(p_xsig, 0u, p_xempty);
                 // mask: prefix columns are visible to every row; only blocks reaching
-                // the tree columns (at most two per split) read mask words
+                // the tree columns (at most two per split) read mask words.  Rows past
+                // the tile's last valid row carry Q = 0 (finite scores) and are never
+                // stored, so they follow whichever path their block takes.
                 const int c0 = c_begin + j * kNb;
                 float mb = -INFINITY;
-                if (row_valid && c0 + kNb <= min(P, c_end)) {
+                if (c0 + kNb <= min(P, c_end)) {
 #pragma unroll
-                    for (int k = 0; k < kNb; ++k) {
-                        sv[k] *= sc;
-                        mb = fmaxf(mb, sv[k]);
-                    }
+                    for (int k = 0; k < kNb; ++k) mb = fmaxf(mb, sv[k]);
                 } else {
-                    uint32_t mw[4] = {0u, 0u, 0u, 0u};  // words covering columns [32*(c0/32), +128)
-                    const int w0 = c0 >> 5;
-                    if (row_valid) {
+                    // 96-bit visibility window of this row starting at column c0:
+                    // mask bits, or-ed with the prefix, and-ed with the split's range
+                    const int w0 = c0 >> 5, sh = c0 & 31;
+                    uint32_t mw[4];
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            if (w0 + t < W) mw[t] = mrow[w0 + t];
+                    for (int t = 0; t < 4; ++t) mw[t] = (w0 + t < W) ? mrow[w0 + t] : 0u;
+                    const int npre = max(0, min(kNb, P - c0));       // leading prefix columns
+                    const int nin = max(0, min(kNb, c_end - c0));    // columns inside the split
+                    uint32_t vbits[3];
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        uint32_t v = __funnelshift_r(mw[t], mw[t + 1], sh);
+                        const int lo = 32 * t;
+                        const uint32_t pre = npre >= lo + 32 ? 0xffffffffu : (npre > lo ? (1u << (npre - lo)) - 1u : 0u);
+                        const uint32_t in = nin >= lo + 32 ? 0xffffffffu : (nin > lo ? (1u << (nin - lo)) - 1u : 0u);
+                        vbits[t] = (v | pre) & in;
                     }
 #pragma unroll
                     for (int k = 0; k < kNb; ++k) {
-                        const int c = c0 + k;
-                        const int rel = c - 32 * w0;  // 0 .. 126
-                        const uint32_t word = rel < 32 ? mw[0] : (rel < 64 ? mw[1] : (rel < 96 ? mw[2] : mw[3]));
-                        const bool vis = row_valid && c < c_end && (c < P || ((word >> (rel & 31)) & 1u));
-                        sv[k] = vis ? sv[k] * sc : -INFINITY;
+                        sv[k] = ((vbits[k >> 5] >> (k & 31)) & 1u) ? sv[k] : -INFINITY;
                         mb = fmaxf(mb, sv[k]);
                     }
                 }
+                mb *= sc;  // scores in log2 units: s * scale * log2(e)
                 float alpha = 1.0f;
                 if (mb > m_ref + 8.0f) {  // also true for the first visible block (m_ref = -inf)
                     alpha = ex2(m_ref - mb);  // 0 when nothing was seen before
@@ -502,27 +547,32 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;  // all -inf rows give p = 0
 #pragma unroll
                 for (int k = 0; k < kNb; k += 2) {
-                    const float p0 = ex2(sv[k] - mref), p1 = ex2(sv[k + 1] - mref);
+                    const float p0 = ex2(fmaf(sv[k], sc, -mref)), p1 = ex2(fmaf(sv[k + 1], sc, -mref));
                     lsum += p0 + p1;
                     pw[k / 2] = pack_bf16(p0, p1);
                 }
                 l += lsum;
-                // both CTAs' P buffer s must be free (PV two blocks back done in both)
-                if (j >= 2 && !wait_or_abort(bar(B_PEMPTY0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-                const uint32_t pbuf = kOffP + s * kPBytes;
+                // both CTAs' P buffer must be free (PV_{j-1} done in both)
+                if (j >= 1 && !wait_or_abort(bar(B_PEMPTY), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
                 const uint32_t p_pin = map_to_cta(bar(B_PIN0 + s), peer);
 #pragma unroll
-                for (int q = 0; q < 12; ++q) {  // 12 chunks of 8 kv, 128-byte swizzle
-                    const uint32_t off = pbuf + (q >> 3) * (kRows * 128) + (r >> 3) * 1024 +
-                                         (r & 7) * 128 + (((q & 7) ^ (r & 7)) << 4);
+                for (int q = 0; q < 12; ++q) {  // 12 chunks of 8 kv
+                    const uint32_t off = (q < 8)
+                        ? kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4)
+                        : kOffP + kP0Bytes + (r >> 3) * 512 + (r & 7) * 64 + (((q - 8) ^ ((r >> 1) & 3)) << 4);
                     *reinterpret_cast<uint4 *>(smem + off) =
                         make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-                    st_async_v4(peer_base + off, pw[4 * q], pw[4 * q + 1], pw[4 * q + 2],
-                                pw[4 * q + 3], p_pin);
                 }
                 st_async_b32(peer_base + kOffAlpha + (s * 64 + xrow) * 4,
                              __float_as_uint(j == 0 ? 1.0f : alpha), p_pin);
-                fence_proxy_async_smem();  // local P rows, read by the tensor core
+                fence_proxy_async_smem();  // P rows: read by the tensor core and the bulk copy
+                __syncwarp();
+                if (lane == 0) {  // this warp's 32 rows to the partner: 4 KB + 2 KB
+                    const uint32_t r0 = (uint32_t)(warp * 32);
+                    bulk_copy_to_cta(peer_base + kOffP + r0 * 128, sbase + kOffP + r0 * 128, 32 * 128, p_pin);
+                    bulk_copy_to_cta(peer_base + kOffP + kP0Bytes + r0 * 64, sbase + kOffP + kP0Bytes + r0 * 64,
+                                     32 * 64, p_pin);
+                }
                 if (!finish_block(j, alpha)) { ok = false; break; }
             }
         }

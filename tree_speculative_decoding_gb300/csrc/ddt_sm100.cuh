@@ -77,6 +77,17 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a, 
                  : "memory");
 }
 
+// bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory into another CTA's, completing `bytes` on its barrier
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                 uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(cluster_bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -127,16 +138,19 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor: start address, leading / stride byte
-// offsets, descriptor version 1, layout (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// offsets, descriptor version 1, layout (2 = 128-byte swizzle, 4 = 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t layout = 2) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;
-    d |= 2ull << 61;
+    d |= (uint64_t)layout << 61;
     return d;
 }
+constexpr uint32_t kSwizzle128B = 2;  // 8 rows x 128 B atoms, chunk ^= row % 8
+constexpr uint32_t kSwizzle64B = 4;   // 8 rows x 64 B atoms,  chunk ^= (row / 2) % 4
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) |

@@ -46,7 +46,9 @@ __device__ __forceinline__ int path_rank(uint32_t path, int depth) {  // rank at
 }
 
 // One warp per request.  The frontier (candidates not yet popped) lives in
-// registers, SLOTS entries per lane; each pop is a warp-wide max.
+// registers, SLOTS entries per lane; each pop is a warp-wide max.  The
+// request's top-k log-probs and ids are staged in shared memory first so no
+// pop waits on a global load.
 __global__ void __launch_bounds__(32)
 build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict__ topk_ids,
                   const int32_t *__restrict__ root_id, const int32_t *__restrict__ budget,
@@ -54,6 +56,7 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
                   int32_t *__restrict__ node_token, int32_t *__restrict__ parent,
                   int32_t *__restrict__ depth, unsigned int *err) {
     __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t ids[DDT_MAX_DEPTH * DDT_MAX_TOPK];
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     const float *lpb = topk_logp + (size_t)b * max_depth * K;
@@ -63,6 +66,7 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
     for (int e = lane; e < max_depth * K; e += 32) {
         float v = lpb[e];
         lp[e] = v;
+        ids[e] = idb[e];
         if ((e % K) > 0 && !(v <= lpb[e - 1])) sorted_ok = false;  // also rejects NaN
         if ((e % K) == 0 && v != v) sorted_ok = false;
     }
@@ -128,7 +132,7 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s)
                 if (s == bs) { my_pout = pout[s]; my_pscore = pscore[s]; }
-            node_token[base + n] = idb[(d - 1) * K + r];
+            node_token[base + n] = ids[(d - 1) * K + r];
             parent[base + n] = my_pout;
             depth[base + n] = d;
             uint64_t sib = 0;  // next sibling: same parent, so pscore / pout stay
