@@ -334,12 +334,12 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
             while (np < nblk) {
                 if (*abort_flag) break;
                 bool did = false;
-                if (ns < nblk && mbar_try_wait(bar(B_FULL0 + ns % kStages), (ns / kStages) & 1) &&
-                    (ns == 0 || mbar_try_wait(bar(B_SFREE), (ns - 1) & 1))) {
+                if (ns < nblk && mbar_test_wait(bar(B_FULL0 + ns % kStages), (ns / kStages) & 1) &&
+                    (ns == 0 || mbar_test_wait(bar(B_SFREE), (ns - 1) & 1))) {
                     issue_s(ns++);
                     did = true;
                 }
-                if (np < ns && mbar_try_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)) {
+                if (np < ns && mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)) {
                     issue_pv(np++);
                     did = true;
                 }
@@ -429,8 +429,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 // uniform readiness tests (tcgen05.ld below is warp-collective)
                 bool can_send = false;
                 if (nsend < nblk && nsend <= nfin + 1) {
-                    bool t = mbar_try_wait(bar(B_SFULL), nsend & 1) &&
-                             (nsend == 0 || mbar_try_wait(bar(B_XEMPTY), (nsend - 1) & 1));
+                    bool t = mbar_test_wait(bar(B_SFULL), nsend & 1) &&
+                             (nsend == 0 || mbar_test_wait(bar(B_XEMPTY), (nsend - 1) & 1));
                     can_send = __shfl_sync(0xffffffffu, t, 0);
                 }
                 if (can_send) {
@@ -466,7 +466,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                         if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
                         pin_armed = true;
                     }
-                    const bool t = __shfl_sync(0xffffffffu, mbar_try_wait(bar(B_PIN0 + s), (nfin >> 1) & 1), 0);
+                    const bool t = __shfl_sync(0xffffffffu, mbar_test_wait(bar(B_PIN0 + s), (nfin >> 1) & 1), 0);
                     if (t) {
                         fence_proxy_async_smem();  // P rows written by the partner, read by the tensor core
                         const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
