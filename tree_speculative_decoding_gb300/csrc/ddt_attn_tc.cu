@@ -16,20 +16,22 @@
 //     one kv split.  CTA c keeps in tensor memory the fp32 output for latent
 //     half c (128 lanes x 256 columns) and its half of Q's 576 dims as bf16
 //     (latent [256c, 256c+256) and rope [512+32c, 512+32c+32): 144 columns);
-//     the rest holds the score block (96 columns).  A full-width output tile
+//     the rest holds the score block (64 columns).  A full-width output tile
 //     (512 columns) would leave no room for scores, which is why the latent
 //     dimension is split across the pair.
-//   * Per kv block of 96 columns: two producer warps gather this CTA's half of
-//     the 96 kv rows with 16-byte cp.async copies into a 128-byte-swizzled
-//     stage (three stages); the MMA warp computes partial scores over the dim
-//     half (tcgen05.mma, A = Q from tensor memory, M=128, N=96).  The pair
+//   * Per kv block of 64 columns: two producer warps gather this CTA's half of
+//     the 64 kv rows with 16-byte cp.async copies into a 128-byte-swizzled
+//     stage (four stages); the MMA warp computes partial scores over the dim
+//     half (tcgen05.mma, A = Q from tensor memory, M=128, N=64).  The pair
 //     swaps fp32 partials through distributed shared memory: CTA c owns the
 //     softmax of rows [64c, 64c+64).  The owner adds the two partials, applies
 //     the mask, runs the online softmax (max rescale only when it grows by
 //     more than 2^8), writes P (bf16) locally and bulk-copies its rows to the
 //     partner with the rows' rescale factors.  Each CTA then accumulates
-//     O_c += P V_c (tcgen05.mma, M=128, N=256, K=96, V read as an MN-major
-//     operand straight from the gathered stage).
+//     O_c += P V_c (tcgen05.mma, M=128, N=256, K=64, V read as an MN-major
+//     operand straight from the gathered stage).  P and the partner-partial
+//     buffer are double-buffered, so the owner writes P_{j+1} while PV_j still
+//     reads P_j and the partner sends partials one block ahead.
 //   * Distributed-shared-memory traffic moves at ~20 B/clk per direction only
 //     when a warp's stores cover contiguous 512-byte runs (scattered 16-byte
 //     pieces measured 8-9 B/clk), hence the chunk-major partial buffer and the
@@ -38,8 +40,6 @@
 //     warps 4 and 6 producers, warp 5 MMA issuer.
 //   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
 //     stops, and still meets its partner at the final cluster barrier.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -53,34 +53,33 @@ namespace {
 using namespace sm100;
 
 constexpr int kRows = 128;            // rows per tile (TMEM lanes)
-constexpr int kNb = 96;               // kv columns per block
+constexpr int kNb = 64;               // kv columns per block
 constexpr int kThreads = 224;         // 7 warps
-constexpr int kBoxBytes = kNb * 128;  // 96 rows x 64 bf16, 128-byte swizzle
-constexpr int kRopeBytes = kNb * 64;  // 96 rows x this CTA's 32 rope dims, 64-byte swizzle
+constexpr int kBoxBytes = kNb * 128;  // 64 rows x 64 bf16, 128-byte swizzle
+constexpr int kRopeBytes = kNb * 64;  // 64 rows x this CTA's 32 rope dims, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBytes;  // 4 latent boxes + rope half
-constexpr int kStages = 3;
-// P (128 rows x 96 kv, bf16): kv 0-63 in a 128-byte-swizzle atom column, kv
-// 64-95 in a 64-byte-swizzle one, so the 32 rows of one warp are contiguous in
-// each (4 KB + 2 KB) and go to the partner as two bulk copies.
-constexpr int kP0Bytes = kRows * 128;
-constexpr int kPBytes = kP0Bytes + kRows * 64;
-// partner partial scores: [24 chunks of 4 columns][64 rows] x 16 bytes, so one
+constexpr int kStages = 4;
+// P (128 rows x 64 kv, bf16): one 128-byte-swizzle atom column; the 32 rows of
+// one warp are 4 contiguous KB and go to the partner as one bulk copy.
+constexpr int kPBytes = kRows * 128;
+// partner partial scores: [16 chunks of 4 columns][64 rows] x 16 bytes, so one
 // warp's 16-byte stores for a chunk are 512 contiguous bytes
 constexpr int kXBytes = (kNb / 4) * 64 * 16;
 
 constexpr int kOffStage = 0;
-constexpr int kOffP = kOffStage + kStages * kStageBytes;
-constexpr int kOffX = kOffP + kPBytes;                    // one P buffer
-constexpr int kOffAlpha = kOffX + kXBytes;                // 2 x 64 floats
+constexpr int kOffP = kOffStage + kStages * kStageBytes;  // two P buffers
+constexpr int kOffX = kOffP + 2 * kPBytes;                // two partial buffers
+constexpr int kOffAlpha = kOffX + 2 * kXBytes;            // 2 x 64 floats
 constexpr int kOffLinv = kOffAlpha + 2 * 64 * 4;          // 64 floats
 constexpr int kOffBar = kOffLinv + 64 * 4;
 // barrier slots
 enum {
-    B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_SFULL, B_SFREE, B_XFULL,
-    B_XEMPTY, B_PIN0, B_PIN1, B_PEMPTY, B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
+    B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL = B_EMPTY0 + kStages, B_SFREE,
+    B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
+    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
 };
-constexpr int kOffXsig = kOffBar + B_COUNT * 8;   // 8-byte landing slot of the x_empty signal
-constexpr int kOffHolder = kOffXsig + 8;
+constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // 2 buffers x 2 owner warps: 4-byte "read" signals
+constexpr int kOffHolder = kOffXsig + 16;
 constexpr int kOffAbort = kOffHolder + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -88,7 +87,7 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 // tensor memory columns
 constexpr uint32_t kColO = 0;    // 256: output, latent half
 constexpr uint32_t kColQ = 256;  // 144: Q half (128 latent + 16 rope), bf16 pairs
-constexpr uint32_t kColS = 400;  // 96: partial scores
+constexpr uint32_t kColS = 400;  // 64: partial scores
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -99,6 +98,7 @@ constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + kNb <= kTmemCols, "tensor memory budget");
+static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 
 struct TcParams {
     AttnArgs a;
@@ -115,7 +115,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUtensorMap kv_map) {
+attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const AttnArgs &a = prm.a;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -177,8 +177,14 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
     // ---- setup ----
     if (tid == 0) {
-        const uint32_t counts[B_COUNT] = {64, 64, 64, 1, 1, 1, 1, 4, 2, 2, 2, 2, 2, 4, 4, 1, 2};
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
+        for (int i = 0; i < B_COUNT; ++i) {
+            uint32_t count = 1;  // stage empties, score full, PV done: one MMA commit
+            if (i < B_EMPTY0) count = 64;                       // stage full: 64 producer lanes
+            else if (i == B_SFREE || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
+            else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
+            else if (i == B_FIN) count = 2;
+            mbar_init(bar(i), count);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -200,7 +206,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
     auto zero_scores = [&]() {
         const uint32_t z[32] = {};
 #pragma unroll
-        for (int q = 0; q < 3; ++q) tmem_st32(tmem + lane_off + kColS + 32 * q, z);
+        for (int q = 0; q < kNb / 32; ++q) tmem_st32(tmem + lane_off + kColS + 32 * q, z);
         tmem_wait_st();
     };
     if (warp < 4) {
@@ -239,7 +245,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
     if (warp == 4 || warp == 6) {
         // ================= producers: gather this CTA's five boxes per kv row =================
-        // Warp 4 moves kv rows [0, 48) of each block, warp 6 rows [48, 96).  One
+        // Warp 4 moves kv rows [0, 32) of each block, warp 6 rows [32, 64).  One
         // warp instruction moves one 128-byte box line of four kv rows: lane =
         // 8 * (row within the group of four) + 16-byte chunk.  Chunks land with
         // the 128-byte swizzle (chunk ^ (row & 7)) that the MMA descriptors
@@ -248,39 +254,27 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         const int half = (warp == 4) ? 0 : 1;
         const int sub = lane >> 3, chunk = lane & 7;
         const char *pool = reinterpret_cast<const char *>(a.kv_pool);
-        // slots of this warp's kv rows lane and lane + 32 (lane < 16) of block j;
-        // loaded one block ahead so the index fetch overlaps the wait for a free stage
-        auto fetch_slots = [&](int j, int (&sl)[2]) {
-            const int c0 = c_begin + j * kNb + 48 * half;
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                sl[t] = a.kv_indices[kv0 + min(c0 + lane + 32 * t, c_end - 1)];  // rows past the end reuse a valid one
+        // slot of this warp's kv row `lane` of block j, loaded one block ahead so
+        // the index fetch overlaps the wait for a free stage
+        auto fetch_slot = [&](int j) {
+            return a.kv_indices[kv0 + min(c_begin + j * kNb + 32 * half + lane, c_end - 1)];  // rows past the end reuse a valid one
         };
-        int next_sl[2];
-        fetch_slots(0, next_sl);
+        int next_slot = fetch_slot(0);
         for (int j = 0; j < nblk && !*abort_flag; ++j) {
             const int s = j % kStages, u = j / kStages;
             if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) break;
             const uint32_t stage = sbase + kOffStage + s * kStageBytes;
-            int slot_a, slot_b;
-            {
-                int sl[2] = {next_sl[0], next_sl[1]};
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (sl[t] < 0 || (int64_t)sl[t] >= a.pool_rows) {
-                        latch(a.err, DDT_DEVERR_KV_INDEX);
-                        sl[t] = 0;
-                    }
-                }
-                slot_a = sl[0]; slot_b = sl[1];
+            int mine = next_slot;
+            if (mine < 0 || (int64_t)mine >= a.pool_rows) {
+                latch(a.err, DDT_DEVERR_KV_INDEX);
+                mine = 0;
             }
-            if (j + 1 < nblk) fetch_slots(j + 1, next_sl);
+            if (j + 1 < nblk) next_slot = fetch_slot(j + 1);
 #pragma unroll 4
-            for (int g = 0; g < 12; ++g) {
-                const int kk = 4 * g + sub;          // row within this warp's 48
-                const int k = 48 * half + kk;        // kv row within the block
-                const int mine = (g < 8) ? slot_a : slot_b;  // g < 8 <=> kk < 32, uniform
-                const int slot = __shfl_sync(0xffffffffu, mine, kk & 31);
+            for (int g = 0; g < 8; ++g) {
+                const int kk = 4 * g + sub;          // row within this warp's 32
+                const int k = 32 * half + kk;        // kv row within the block
+                const int slot = __shfl_sync(0xffffffffu, mine, kk);
                 const char *src = pool + (int64_t)slot * (DDT_D * 2) + chunk * 16;
                 const uint32_t dst = stage + (k >> 3) * 1024 + (k & 7) * 128 + ((chunk ^ (k & 7)) << 4);
 #pragma unroll
@@ -314,19 +308,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 mma_commit(bar(B_SFULL));
             };
             auto issue_pv = [&](int k) {
-                const int s = k % kStages;
+                const int s = k % kStages, pb = k & 1;
                 tc_fence_after();
-                const uint32_t pbuf = sbase + kOffP;
+                const uint32_t pbuf = sbase + kOffP + pb * kPBytes;
                 const uint32_t stage = sbase + kOffStage + s * kStageBytes;
 #pragma unroll
                 for (int ks = 0; ks < kNb / 16; ++ks) {
-                    const uint64_t ad = (ks < 4) ? smem_desc(pbuf + ks * 32, 16, 1024)
-                                                 : smem_desc(pbuf + kP0Bytes + (ks - 4) * 32, 16, 512, kSwizzle64B);
+                    const uint64_t ad = smem_desc(pbuf + ks * 32, 16, 1024);
                     const uint64_t bd = smem_desc(stage + ks * 2048, kBoxBytes, 1024);
                     mma_ss(tmem + kColO, ad, bd, kIdescPV, 1u);
                 }
                 mma_commit(bar(B_EMPTY0 + s));
-                mma_commit_multicast(bar(B_PEMPTY), (uint16_t)0x3);
+                mma_commit_multicast(bar(B_PEMPTY0 + pb), (uint16_t)0x3);
                 mma_commit(bar(B_PVDONE));
             };
             int ns = 0, np = 0;  // next S block, next PV block
@@ -364,23 +357,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
         const uint32_t *mrow = a.mask + a.mask_indptr[b] + (int64_t)node * W;
         const float sc = a.scale * kLog2e;
         // cluster addresses of the partner's buffers / barriers
-        const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * 16, peer);
-        const uint32_t p_xfull = map_to_cta(bar(B_XFULL), peer);
-        const uint32_t p_xempty = map_to_cta(bar(B_XEMPTY), peer);
-        const uint32_t p_xsig = map_to_cta(sbase + kOffXsig + 4 * (warp & 1), peer);
         const uint32_t peer_base = map_to_cta(sbase, peer);
         const uint32_t p_fin = map_to_cta(bar(B_FIN), peer);
         const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
 
-        // read S_j into registers and hand the score buffer back to the MMA warp
-        auto load_scores = [&](int j, float (&sv)[kNb]) -> bool {
-            if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) return false;
+        // read S_j into registers, clear it, and hand the score buffer back to the MMA warp
+        auto take_scores = [&](float (&sv)[kNb]) {
             tc_fence_after();
             uint32_t t32[32];
 #pragma unroll
-            for (int q = 0; q < 3; ++q) {
+            for (int q = 0; q < kNb / 32; ++q) {
                 tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
                 tmem_wait_ld();
 #pragma unroll
@@ -390,25 +378,23 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_SFREE));
-            return true;
         };
-        // O row *= alpha once PV_{j-1} is done (needed by both roles before P_j is used)
+        // O row *= alpha before PV_j (only when a row of this warp rescales, which
+        // needs PV_{j-1} finished); then this warp's part of P_j is in place.
         auto finish_block = [&](int j, float alpha) -> bool {
-            if (j > 0) {
-                if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) return false;
+            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (j > 0 && !wait_or_abort(bar(B_PVDONE), (j - 1) & 1, abort_flag, a.err)) return false;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-                    uint32_t t32[32];
+                uint32_t t32[32];
 #pragma unroll 1
-                    for (int q = 0; q < 8; ++q) {
-                        tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
-                        tmem_wait_ld();
+                for (int q = 0; q < 8; ++q) {
+                    tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
-                        tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) t32[e] = __float_as_uint(__uint_as_float(t32[e]) * alpha);
+                    tmem_st32(tmem + lane_off + kColO + 32 * q, t32);
                 }
+                tmem_wait_st();
             }
             tc_fence_before();
             __syncwarp();
@@ -418,8 +404,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 
         if (!owner) {
             // Rows owned by the partner: send each block's partial scores as soon as
-            // they exist and take the partner's P rows (and rescale factor) as soon
-            // as they land -- whichever is ready first; at most one send ahead.
+            // they exist (two partial buffers: up to two sends ahead) and take the
+            // partner's P rows (and rescale factors) as soon as they land.
+            const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * 16, peer);
             int nsend = 0, nfin = 0;
             bool pin_armed = false;
             uint32_t idle = 0;
@@ -428,47 +415,33 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                 bool did = false;
                 // uniform readiness tests (tcgen05.ld below is warp-collective)
                 bool can_send = false;
-                if (nsend < nblk && nsend <= nfin + 1) {
+                if (nsend < nblk && nsend <= nfin + 2) {
                     bool t = mbar_test_wait(bar(B_SFULL), nsend & 1) &&
-                             (nsend == 0 || mbar_test_wait(bar(B_XEMPTY), (nsend - 1) & 1));
+                             (nsend < 2 || mbar_test_wait(bar(B_XEMPTY0 + (nsend & 1)), ((nsend - 2) >> 1) & 1));
                     can_send = __shfl_sync(0xffffffffu, t, 0);
                 }
                 if (can_send) {
                     const int j = nsend++;
                     float sv[kNb];
-                    tc_fence_after();
-                    {
-                        uint32_t t32[32];
-#pragma unroll
-                        for (int q = 0; q < 3; ++q) {
-                            tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
-                        }
-                    }
-                    zero_scores();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_SFREE));
+                    take_scores(sv);
+                    const uint32_t dst = px_row + (j & 1) * kXBytes;
+                    const uint32_t p_xfull = map_to_cta(bar(B_XFULL0 + (j & 1)), peer);
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q)
-                        st_async_v4(px_row + 64 * 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
+                        st_async_v4(dst + 64 * 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
                                     __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
                     // the owner signals "read" with a 4-byte store per owner warp
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY), 4);
-                    (void)j;
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY0 + (j & 1)), 4);
                     did = true;
                 }
                 if (nfin < nsend) {
                     const int s = nfin & 1;
                     if (!pin_armed) {
-                        if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * (12 * 16 + 4));
+                        if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * ((kNb / 8) * 16 + 4));
                         pin_armed = true;
                     }
                     const bool t = __shfl_sync(0xffffffffu, mbar_test_wait(bar(B_PIN0 + s), (nfin >> 1) & 1), 0);
                     if (t) {
-                        fence_proxy_async_smem();  // P rows written by the partner, read by the tensor core
                         const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
                         if (!finish_block(nfin, alpha)) { ok = false; break; }
                         ++nfin;
@@ -488,12 +461,13 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
             for (int j = 0; j < nblk && ok; ++j) {
                 const int s = j & 1;
                 float sv[kNb];
-                if (!load_scores(j, sv)) { ok = false; break; }
+                if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
+                take_scores(sv);
                 // owner: partner partial + own partial -> softmax -> P for both CTAs
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL), 32 * kNb * 4);
-                if (!wait_or_abort(bar(B_XFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + s), 32 * kNb * 4);
+                if (!wait_or_abort(bar(B_XFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
                 {
-                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX) + xrow;
+                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + s * kXBytes) + xrow;
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q) {
                         const float4 v = x[64 * q];
@@ -501,7 +475,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                     }
                 }
                 __syncwarp();
-                if (lane == 0) st_async_b32(p_xsig, 0u, p_xempty);
+                if (lane == 0)
+                    st_async_b32(map_to_cta(sbase + kOffXsig + 4 * (2 * s + (warp & 1)), peer), 0u,
+                                 map_to_cta(bar(B_XEMPTY0 + s), peer));
                 // mask: prefix columns are visible to every row; only blocks reaching
                 // the tree columns (at most two per split) read mask words.  Rows past
                 // the tile's last valid row carry Q = 0 (finite scores) and are never
@@ -512,18 +488,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
 #pragma unroll
                     for (int k = 0; k < kNb; ++k) mb = fmaxf(mb, sv[k]);
                 } else {
-                    // 96-bit visibility window of this row starting at column c0:
+                    // 64-bit visibility window of this row starting at column c0:
                     // mask bits, or-ed with the prefix, and-ed with the split's range
                     const int w0 = c0 >> 5, sh = c0 & 31;
-                    uint32_t mw[4];
+                    uint32_t mw[3];
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) mw[t] = (w0 + t < W) ? mrow[w0 + t] : 0u;
+                    for (int t = 0; t < 3; ++t) mw[t] = (w0 + t < W) ? mrow[w0 + t] : 0u;
                     const int npre = max(0, min(kNb, P - c0));       // leading prefix columns
                     const int nin = max(0, min(kNb, c_end - c0));    // columns inside the split
-                    uint32_t vbits[3];
+                    uint32_t vbits[2];
 #pragma unroll
-                    for (int t = 0; t < 3; ++t) {
-                        uint32_t v = __funnelshift_r(mw[t], mw[t + 1], sh);
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t v = __funnelshift_r(mw[t], mw[t + 1], sh);
                         const int lo = 32 * t;
                         const uint32_t pre = npre >= lo + 32 ? 0xffffffffu : (npre > lo ? (1u << (npre - lo)) - 1u : 0u);
                         const uint32_t in = nin >= lo + 32 ? 0xffffffffu : (nin > lo ? (1u << (nin - lo)) - 1u : 0u);
@@ -552,14 +528,16 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                     pw[k / 2] = pack_bf16(p0, p1);
                 }
                 l += lsum;
-                // both CTAs' P buffer must be free (PV_{j-1} done in both)
-                if (j >= 1 && !wait_or_abort(bar(B_PEMPTY), (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                // both CTAs' P buffer s must be free (PV_{j-2} done in both)
+                if (j >= 2 && !wait_or_abort(bar(B_PEMPTY0 + s), ((j - 2) >> 1) & 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t p_pin = map_to_cta(bar(B_PIN0 + s), peer);
+                const uint32_t poff = kOffP + s * kPBytes;
 #pragma unroll
-                for (int q = 0; q < 12; ++q) {  // 12 chunks of 8 kv
-                    const uint32_t off = (q < 8)
-                        ? kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4)
-                        : kOffP + kP0Bytes + (r >> 3) * 512 + (r & 7) * 64 + (((q - 8) ^ ((r >> 1) & 3)) << 4);
+                for (int q = 0; q < kNb / 8; ++q) {  // chunks of 8 kv, 128-byte swizzle
+                    const uint32_t off = poff + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(smem + off) =
                         make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
                 }
@@ -567,17 +545,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
                              __float_as_uint(j == 0 ? 1.0f : alpha), p_pin);
                 fence_proxy_async_smem();  // P rows: read by the tensor core and the bulk copy
                 __syncwarp();
-                if (lane == 0) {  // this warp's 32 rows to the partner: 4 KB + 2 KB
-                    const uint32_t r0 = (uint32_t)(warp * 32);
-                    bulk_copy_to_cta(peer_base + kOffP + r0 * 128, sbase + kOffP + r0 * 128, 32 * 128, p_pin);
-                    bulk_copy_to_cta(peer_base + kOffP + kP0Bytes + r0 * 64, sbase + kOffP + kP0Bytes + r0 * 64,
-                                     32 * 64, p_pin);
+                if (lane == 0) {  // this warp's 32 rows to the partner
+                    const uint32_t off = poff + (uint32_t)(warp * 32) * 128;
+                    bulk_copy_to_cta(peer_base + off, sbase + off, 32 * 128, p_pin);
                 }
-                if (!finish_block(j, alpha)) { ok = false; break; }
+                if (!finish_block(j, j == 0 ? 1.0f : alpha)) { ok = false; break; }  // O starts at zero
             }
         }
 
         // ---- epilogue: O_c / l into the output (or this split's partial) ----
+        // PV_{nblk-2} may still be running here (P is double-buffered), and a
+        // parity wait only tells apart phases one apart: wait for both in order.
+        if (ok && nblk >= 2 && !wait_or_abort(bar(B_PVDONE), (nblk - 2) & 1, abort_flag, a.err)) ok = false;
         if (ok && wait_or_abort(bar(B_PVDONE), (nblk - 1) & 1, abort_flag, a.err)) {
             float linv = 0.f;
             float lse_v = -INFINITY;
@@ -634,20 +613,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUt
     }
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
 }  // namespace
 
 cudaError_t attn_tc_prepare_device() {
-    if (!g_encode) {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
     return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemBytes);
 }
@@ -672,22 +640,11 @@ int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, 
 }
 
 cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
-    if (!g_encode) return cudaErrorInitializationError;
-    CUtensorMap map;
-    cuuint64_t dims[2] = {(cuuint64_t)DDT_D, (cuuint64_t)a.pool_rows};
-    cuuint64_t strides[1] = {(cuuint64_t)DDT_D * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult cr = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                           const_cast<uint16_t *>(a.kv_pool), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     TcParams prm;
     prm.a = a;
     prm.tiles_per_req = (a.max_q_len * a.num_heads + kRows - 1) / kRows;
     dim3 grid(2 * a.num_splits, prm.tiles_per_req, a.batch);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(prm, map);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(prm);
     return cudaGetLastError();
 }
 
