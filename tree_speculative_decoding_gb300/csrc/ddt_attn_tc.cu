@@ -36,8 +36,9 @@
 //     when a warp's stores cover contiguous 512-byte runs (scattered 16-byte
 //     pieces measured 8-9 B/clk), hence the chunk-major partial buffer and the
 //     bulk-copied P rows.
-//   * Warp roles: warps 0-3 softmax / epilogue (thread = row = TMEM lane),
-//     warps 4 and 6 producers, warp 5 MMA issuer.
+//   * Warp roles: warps 0-3 softmax / epilogue (thread = row = TMEM lane);
+//     of warps 4-6, one issues the MMAs (placed next to a non-owner softmax
+//     warp) and two are producers.
 //   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
 //     stops, and still meets its partner at the final cluster barrier.
 #include <cuda_runtime.h>
@@ -91,6 +92,11 @@ constexpr uint32_t kColS = 400;  // 64: partial scores
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;
+// Lazy rescale: the running max m (log2 units) moves only when a block's max
+// exceeds it by more than this, so p = 2^(s - m) <= 2^20 -- far inside bf16 and
+// fp32 range -- while a rescale of O (a serial 256-column TMEM read-modify-
+// write, ~0.7 us) stays rare.
+constexpr float kRescaleLog2 = 20.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kIdescS = idesc_bf16(kRows, kNb, 0, 0);
@@ -237,13 +243,17 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     }
     // Q / O / S in tensor memory before the first MMA: the softmax warps and the
     // MMA warp meet on a named barrier; the producers start gathering at once.
-    if (warp < 4 || warp == 5) {
+    // Warp w issues on sub-partition w % 4.  The MMA warp spins on barriers, so
+    // it goes next to a non-owner softmax warp: warp 6 (with warp 2) in rank 0,
+    // where warps 0-1 own rows, and warp 4 (with warp 0) in rank 1.
+    const int mma_warp = rank ? 4 : 6;
+    if (warp < 4 || warp == mma_warp) {
         tc_fence_before();
         named_barrier(1, 160);
         tc_fence_after();
     }
 
-    if (warp == 4 || warp == 6) {
+    if (warp >= 4 && warp != mma_warp) {
         // ================= producers: gather this CTA's five boxes per kv row =================
         // Warp 4 moves kv rows [0, 32) of each block, warp 6 rows [32, 64).  One
         // warp instruction moves one 128-byte box line of four kv rows: lane =
@@ -251,7 +261,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         // the 128-byte swizzle (chunk ^ (row & 7)) that the MMA descriptors
         // expect.  Each lane arrives on the stage barrier once its own copies
         // have landed (64 arrivals per stage).
-        const int half = (warp == 4) ? 0 : 1;
+        const int half = (warp == (rank ? 5 : 4)) ? 0 : 1;
         const int sub = lane >> 3, chunk = lane & 7;
         const char *pool = reinterpret_cast<const char *>(a.kv_pool);
         // slot of this warp's kv row `lane` of block j, loaded one block ahead so
@@ -286,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             }
             cp_async_arrive(bar(B_FULL0 + s));
         }
-    } else if (warp == 5) {
+    } else if (warp == mma_warp) {
         // ================= MMA issuer =================
         // Issues S_j as soon as block j is loaded and the score buffer is free,
         // and PV_j as soon as P_j is in place -- whichever is ready first.
@@ -342,6 +352,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     *abort_flag = 1;
                     latch(a.err, DDT_DEVERR_TIMEOUT);
                     break;
+                } else {
+                    __nanosleep(32);  // leave the issue slot to the softmax warp on this sub-partition
                 }
             }
         }
@@ -455,6 +467,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     *abort_flag = 1;
                     latch(a.err, DDT_DEVERR_TIMEOUT);
                     ok = false;
+                } else {
+                    __nanosleep(32);
                 }
             }
         } else {
@@ -513,7 +527,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 }
                 mb *= sc;  // scores in log2 units: s * scale * log2(e)
                 float alpha = 1.0f;
-                if (mb > m_ref + 8.0f) {  // also true for the first visible block (m_ref = -inf)
+                if (mb > m_ref + kRescaleLog2) {  // also true for the first visible block (m_ref = -inf)
                     alpha = ex2(m_ref - mb);  // 0 when nothing was seen before
                     l *= alpha;
                     m_ref = mb;
