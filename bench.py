@@ -37,7 +37,33 @@ if ROOT not in sys.path:
 
 WORKLOAD = "single_p4096_b32_h64"
 METRIC = "verify-attn TFLOP/s and KV GB/s per step, % of roofline, 1xGB300"
-PROFILE_TRAFFIC = None  # dram bytes per ddt_verify_attn call from ncu; null until captured
+# DRAM bytes (read + write) of one ddt_verify_attn call (partial + combine kernels) on
+# this workload, from ncu (profiles/attn_tc_single_p4096_b32_h64.md), valid only for the
+# kernel sources it was taken from: a change to them turns the field back to null.
+PROFILE_TRAFFIC = {
+    "bytes": 7308800 + 22016 + 17347840 + 0,
+    "sources": {
+        "tree_speculative_decoding_gb300/csrc/ddt_attn_tc.cu":
+            "b3216c5861871b3f465436b8460ec802ee1c7fa6f04c6485e52ee41d256986ed",
+        "tree_speculative_decoding_gb300/csrc/ddt_attn_combine.cu":
+            "f276828594fc64a5ce3a9878d6c94e4ee6ccd4a2b9d072fd4e61320ef27e84d4",
+        "tree_speculative_decoding_gb300/csrc/ddt_sm100.cuh":
+            "14789d6e497933ab00d5c228a740828f625e9726a881f78f16b8853c1cf9ec08",
+    },
+}
+
+
+def profiled_traffic():
+    """The profiled DRAM bytes if the attention sources are unchanged since, else None."""
+    import hashlib
+    for rel, digest in PROFILE_TRAFFIC["sources"].items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return PROFILE_TRAFFIC["bytes"]
 
 
 def measured_peaks():
@@ -263,7 +289,7 @@ def run_device(args, rank, world, local_rank):
         "verify_attn_ms": round(attn_mean_ms, 5),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4),
-                     "traffic": PROFILE_TRAFFIC, "peak_source": f"{peak_kind} bf16 burst",
+                     "traffic": profiled_traffic(), "peak_source": f"{peak_kind} bf16 burst",
                      "kernel": "ddt_verify_attn (partial + combine)",
                      "t_roof_ms": round(t_roof_ms, 5),
                      "frac_of_sustained": round(achieved / tf_sus, 4)},
