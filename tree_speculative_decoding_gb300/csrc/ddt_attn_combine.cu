@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kThreads)
 attn_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                     int num_splits, int64_t rows, float *__restrict__ out,
                     float *__restrict__ lse) {
+    pdl_trigger();
+    pdl_wait();  // the partials come from the partial pass
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     float m = -INFINITY;
@@ -55,9 +57,8 @@ attn_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s) {
     const int64_t rows = (int64_t)a.total_q * a.num_heads;
     if (rows == 0) return cudaSuccess;
-    attn_combine_kernel<<<(unsigned)rows, kThreads, 0, s>>>(a.o_part, a.lse_part, a.num_splits,
-                                                            rows, a.out, a.lse);
-    return cudaGetLastError();
+    return launch_pdl(attn_combine_kernel, dim3((unsigned)rows), dim3(kThreads), 0, s, a.o_part,
+                      a.lse_part, a.num_splits, rows, a.out, a.lse);
 }
 
 }  // namespace ddt

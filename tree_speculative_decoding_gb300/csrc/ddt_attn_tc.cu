@@ -134,6 +134,11 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // The next kernel (the combine) may be scheduled now.  This kernel reads only
+    // caller inputs until it needs mask words (the visibility compile may still be
+    // running: prefix blocks never read the mask) or writes its outputs; both
+    // happen after pdl_wait().
+    pdl_trigger();
     const uint32_t rank = cluster_ctarank();  // 0 or 1: latent half
     const uint32_t peer = rank ^ 1u;
     const int split = blockIdx.x >> 1;
@@ -148,7 +153,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const int N = a.kv_indptr[b + 1] - kv0;
     const int rows_req = T * H;
     const int row0 = tile * kRows;
-    if (row0 >= rows_req) return;  // uniform in the pair: no cluster interaction yet
+    if (row0 >= rows_req) { pdl_wait(); return; }  // uniform in the pair: no cluster interaction yet
     bool bad = false;
     if (T > a.max_q_len || T < 1) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_QO_INDPTR); }
     if (N < T || N > a.max_kv_len) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_KV_INDPTR); }
@@ -158,7 +163,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         bad = true;
         if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_MASK_INDPTR);
     }
-    if (bad) return;  // uniform in the pair
+    if (bad) { pdl_wait(); return; }  // uniform in the pair
     const int rows_valid = min(kRows, rows_req - row0);
     const int i_max = (row0 + rows_valid - 1) / H;   // last node in the tile
     const int kv_end = P + i_max + 1;                 // nothing beyond is visible to the tile
@@ -168,6 +173,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const int64_t rows_total = (int64_t)a.total_q * H;
 
     if (nblk == 0) {  // empty split: neutral partial result (only happens with splits > 1)
+        pdl_wait();
         if (warp < 4) {
             const int r = tid;
             if (r < rows_valid && a.num_splits > 1) {
@@ -374,6 +380,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        bool mask_ready = false;
 
         // read S_j into registers, clear it, and hand the score buffer back to the MMA warp
         auto take_scores = [&](float (&sv)[kNb]) {
@@ -502,6 +509,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
 #pragma unroll
                     for (int k = 0; k < kNb; ++k) mb = fmaxf(mb, sv[k]);
                 } else {
+                    if (!mask_ready) {  // the mask is the visibility compile's output
+                        pdl_wait();
+                        mask_ready = true;
+                    }
                     // 64-bit visibility window of this row starting at column c0:
                     // mask bits, or-ed with the prefix, and-ed with the split's range
                     const int w0 = c0 >> 5, sh = c0 & 31;
@@ -572,6 +583,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         // parity wait only tells apart phases one apart: wait for both in order.
         if (ok && nblk >= 2 && !wait_or_abort(bar(B_PVDONE), (nblk - 2) & 1, abort_flag, a.err)) ok = false;
         if (ok && wait_or_abort(bar(B_PVDONE), (nblk - 1) & 1, abort_flag, a.err)) {
+            pdl_wait();  // the previous kernel may still read this step's output buffers
             float linv = 0.f;
             float lse_v = -INFINITY;
             bool have = true;
@@ -618,6 +630,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     }
 
     // ---- teardown: nobody leaves while the partner may still write here ----
+    pdl_wait();  // every path waits once, so this grid ends after the previous one
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -658,8 +671,7 @@ cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
     prm.a = a;
     prm.tiles_per_req = (a.max_q_len * a.num_heads + kRows - 1) / kRows;
     dim3 grid(2 * a.num_splits, prm.tiles_per_req, a.batch);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(prm);
-    return cudaGetLastError();
+    return launch_pdl(attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, prm);
 }
 
 }  // namespace ddt

@@ -14,6 +14,38 @@ __device__ __forceinline__ void latch(unsigned int *err, unsigned int bit) {
     if (err) atomicOr(err, bit);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization and announces at its start that the next
+// kernel in the stream may be scheduled.  A kernel therefore may run while the
+// previous one is still running, and it calls pdl_wait() -- which returns once
+// the previous kernel (and, transitively, everything before it) has finished
+// and its writes are visible -- before it reads anything an earlier kernel of
+// the step wrote, and before its first global write.  Work on the caller's
+// inputs (q, the kv pool and indices, top-k) may happen before the wait; a
+// kernel that does not itself trigger early is complete before any of ours
+// starts.  Dependents are scheduled only after every CTA of the previous
+// kernel has started, so no wait can hold resources the previous kernel needs.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Launchers (host functions; each enqueues on `s` and returns the launch error).
 cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
                               const int32_t *root_id, const int32_t *budget,

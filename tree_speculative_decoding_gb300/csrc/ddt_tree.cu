@@ -46,9 +46,14 @@ __device__ __forceinline__ int path_rank(uint32_t path, int depth) {  // rank at
 }
 
 // One warp per request.  The frontier (candidates not yet popped) lives in
-// registers, SLOTS entries per lane; each pop is a warp-wide max.  The
-// request's top-k log-probs and ids are staged in shared memory first so no
-// pop waits on a global load.
+// registers, SLOTS entries per lane, with the request's top-k log-probs and ids
+// staged in shared memory.  Each pop is a warp-wide max over 64-bit keys.  To
+// keep the sequential chain short, every lane prepares, before the reduction,
+// what its best candidate would produce if it won (its token, its next
+// sibling's key, its best child's key); the winner then refills its own slot
+// with the child (or the sibling) and hands the remaining candidate to lane
+// n % 32, which always has a free slot: lane k receives candidates only at pops
+// n = k, k+32, k+64, k+96 (n <= budget <= 127), at most 4 including the seed.
 __global__ void __launch_bounds__(32)
 build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict__ topk_ids,
                   const int32_t *__restrict__ root_id, const int32_t *__restrict__ budget,
@@ -57,121 +62,140 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
                   int32_t *__restrict__ depth, unsigned int *err) {
     __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
     __shared__ int32_t ids[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t out_tok[DDT_MAX_Q_LEN], out_par[DDT_MAX_Q_LEN], out_dep[DDT_MAX_Q_LEN];
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
-    const float *lpb = topk_logp + (size_t)b * max_depth * K;
-    const int32_t *idb = topk_ids + (size_t)b * max_depth * K;
-
-    bool sorted_ok = true;
-    for (int e = lane; e < max_depth * K; e += 32) {
-        float v = lpb[e];
-        lp[e] = v;
+    pdl_trigger();
+    // independent loads first, so their latencies overlap (caller inputs: no wait needed)
+    const int base = qo_indptr[b];
+    const int end = qo_indptr[b + 1];
+    const int nb = budget[b];
+    const int rid = root_id[b];
+    const int total = max_depth * K;
+    const float *lpb = topk_logp + (size_t)b * total;
+    const int32_t *idb = topk_ids + (size_t)b * total;
+    for (int e = lane; e < total; e += 32) {
+        lp[e] = lpb[e];
         ids[e] = idb[e];
-        if ((e % K) > 0 && !(v <= lpb[e - 1])) sorted_ok = false;  // also rejects NaN
-        if ((e % K) == 0 && v != v) sorted_ok = false;
     }
     __syncwarp();
+    bool sorted_ok = true;
+    for (int e = lane; e < total; e += 32) {
+        const float v = lp[e];
+        if ((e % K) > 0 ? !(v <= lp[e - 1]) : (v != v)) sorted_ok = false;  // also rejects NaN
+    }
     if (__any_sync(FULL, !sorted_ok)) {
+        pdl_wait();
         if (lane == 0) latch(err, DDT_DEVERR_TOPK_ORDER);
         return;
     }
-
-    const int base = qo_indptr[b];
-    const int nb = budget[b];
-    if (nb < 0 || nb > DDT_MAX_Q_LEN - 1 || qo_indptr[b + 1] - base != nb + 1) {
+    if (nb < 0 || nb > DDT_MAX_Q_LEN - 1 || end - base != nb + 1) {
+        pdl_wait();
         if (lane == 0) latch(err, DDT_DEVERR_QO_INDPTR);
         return;
     }
     if (lane == 0) {
-        node_token[base] = root_id[b];
-        parent[base] = -1;
-        depth[base] = 0;
+        out_tok[0] = rid;
+        out_par[0] = -1;
+        out_dep[0] = 0;
     }
-    if (nb == 0) return;
 
+    if (nb == 0) {
+        pdl_wait();
+        if (lane == 0) { node_token[base] = rid; parent[base] = -1; depth[base] = 0; }
+        return;
+    }
     uint64_t key[SLOTS];
     float pscore[SLOTS];  // score of the candidate's parent (for its next sibling)
     int pout[SLOTS];      // output index of the candidate's parent
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) { key[s] = 0; pscore[s] = 0.f; pout[s] = 0; }
-    if (lane == 0) {  // seed: rank-0 child of the root
-        key[0] = make_key(0.0f + lp[0], 1, 0u);
-        pscore[0] = 0.0f;
-        pout[0] = 0;
-    }
+    if (lane == 0) key[0] = make_key(0.0f + lp[0], 1, 0u);  // seed: rank-0 child of the root
 
-    for (int n = 1; n <= nb; ++n) {
-        // lane-local best
-        uint64_t best = 0;
-        int bs = 0;
+    // this lane's best candidate and what it yields if popped
+    uint64_t best = 0, sib = 0, child = 0;
+    int bs = 0, bd = 0, btok = 0, bpout = 0;
+    float bpscore = 0.f, bscore = 0.f;
+    auto prepare = [&]() {
+        best = 0;
+        bs = 0;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s)
             if (key[s] > best) { best = key[s]; bs = s; }
+        sib = 0;
+        child = 0;
+        if (best != 0) {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+                if (s == bs) { bpout = pout[s]; bpscore = pscore[s]; }
+            bd = key_depth(best);
+            const uint32_t path = key_path(best);
+            const int r = path_rank(path, bd);
+            bscore = unorder_score((uint32_t)(best >> 32));
+            btok = ids[(bd - 1) * K + r];
+            if (r + 1 < K)
+                sib = make_key(bpscore + lp[(bd - 1) * K + r + 1], bd, path + (1u << (28 - 4 * bd)));
+            if (bd < max_depth) child = make_key(bscore + lp[bd * K + 0], bd + 1, path);
+        }
+    };
+    prepare();
+
+    for (int n = 1; n <= nb; ++n) {
         const uint32_t hi = (uint32_t)(best >> 32);
         const uint32_t mhi = __reduce_max_sync(FULL, hi);
         if (mhi == 0u) {  // frontier empty: budget exceeds the implicit tree
+            pdl_wait();
             if (lane == 0) latch(err, DDT_DEVERR_EXHAUSTED);
             return;
         }
-        const uint32_t lo = (uint32_t)best;
-        const uint32_t mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
-        const unsigned who = __ballot_sync(FULL, hi == mhi && lo == mlo && best != 0);
-        const int wl = __ffs(who) - 1;
-
-        // winner pops its slot; the sibling (same parent) reuses that slot
-        int cd = 0, has_child = 0;
-        float cscore = 0.f;
-        uint32_t cpath = 0;
-        if (lane == wl) {
-            const int d = key_depth(best);
-            const uint32_t path = key_path(best);
-            const int r = path_rank(path, d);
-            const float score = unorder_score(mhi);
-            int my_pout = 0;
-            float my_pscore = 0.f;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-                if (s == bs) { my_pout = pout[s]; my_pscore = pscore[s]; }
-            node_token[base + n] = ids[(d - 1) * K + r];
-            parent[base + n] = my_pout;
-            depth[base + n] = d;
-            uint64_t sib = 0;  // next sibling: same parent, so pscore / pout stay
-            if (r + 1 < K)
-                sib = make_key(my_pscore + lp[(d - 1) * K + r + 1], d,
-                               path + (1u << (28 - 4 * d)));
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-                if (s == bs) key[s] = sib;
-            if (d < max_depth) {
-                has_child = 1;
-                cd = d + 1;
-                cscore = score + lp[d * K + 0];
-                cpath = path;  // rank 0 at the new depth
-            }
+        unsigned who = __ballot_sync(FULL, hi == mhi);
+        if (__popc(who) > 1) {  // equal scores: the rest of the key decides
+            const uint32_t lo = (uint32_t)best;
+            const uint32_t mlo = __reduce_max_sync(FULL, hi == mhi ? lo : 0u);
+            who = __ballot_sync(FULL, hi == mhi && lo == mlo);
         }
-        has_child = __shfl_sync(FULL, has_child, wl);
-        if (has_child && n < nb) {
-            cd = __shfl_sync(FULL, cd, wl);
-            const float parent_score = __shfl_sync(FULL, unorder_score(mhi), wl);
-            cscore = __shfl_sync(FULL, cscore, wl);
-            cpath = __shfl_sync(FULL, cpath, wl);
-            // first lane with a free slot takes the child
-            int free_slot = -1;
+        const int wl = __ffs(who) - 1;
+        bool extra = false;  // the winner's sibling, when its child took the slot
+        if (lane == wl) {  // outputs go to shared memory; one coalesced write at the end
+            out_tok[n] = btok;
+            out_par[n] = bpout;
+            out_dep[n] = bd;
+            extra = child != 0 && sib != 0;
 #pragma unroll
-            for (int s = SLOTS - 1; s >= 0; --s)
-                if (key[s] == 0) free_slot = s;
-            const unsigned has_free = __ballot_sync(FULL, free_slot >= 0);
-            const int tl = __ffs(has_free) - 1;  // exists: frontier <= budget < 128
-            if (lane == tl) {
+            for (int s = 0; s < SLOTS; ++s)
+                if (s == bs) {
+                    if (child != 0) { key[s] = child; pscore[s] = bscore; pout[s] = n; }
+                    else key[s] = sib;  // same parent: pscore / pout stay
+                }
+        }
+        if (n == nb) break;
+        if (__shfl_sync(FULL, extra ? 1 : 0, wl)) {
+            const uint32_t xhi = __shfl_sync(FULL, (uint32_t)(sib >> 32), wl);
+            const uint32_t xlo = __shfl_sync(FULL, (uint32_t)sib, wl);
+            const float xps = __shfl_sync(FULL, bpscore, wl);
+            const int xpo = __shfl_sync(FULL, bpout, wl);
+            if (lane == (n & 31)) {
+                int free_slot = 0;
+#pragma unroll
+                for (int s = SLOTS - 1; s >= 0; --s)
+                    if (key[s] == 0) free_slot = s;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s)
                     if (s == free_slot) {
-                        key[s] = make_key(cscore, cd, cpath);
-                        pscore[s] = parent_score;
-                        pout[s] = n;
+                        key[s] = ((uint64_t)xhi << 32) | xlo;
+                        pscore[s] = xps;
+                        pout[s] = xpo;
                     }
             }
         }
+        if (lane == wl || lane == (n & 31)) prepare();
+    }
+    __syncwarp();
+    pdl_wait();  // the previous kernel may still read the tree buffers
+    for (int i = lane; i <= nb; i += 32) {
+        node_token[base + i] = out_tok[i];
+        parent[base + i] = out_par[i];
+        depth[base + i] = out_dep[i];
     }
 }
 
@@ -183,6 +207,8 @@ __global__ void compile_visibility_kernel(const int32_t *__restrict__ parent,
                                           const int32_t *__restrict__ mask_indptr, int batch,
                                           int total_words, uint32_t *__restrict__ mask,
                                           unsigned int *err) {
+    pdl_trigger();
+    pdl_wait();  // parent comes from the tree build
     for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < total_words;
          w += gridDim.x * blockDim.x) {
         // request owning word w: last b with mask_indptr[b] <= w
@@ -241,6 +267,8 @@ accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict_
               int32_t *__restrict__ bonus, unsigned int *err) {
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();  // the tree comes from the tree build
     const int width = max_depth + 1;
     const int base = qo_indptr[b];
     const int T = qo_indptr[b + 1] - base;
@@ -292,9 +320,8 @@ cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
                               const int32_t *qo_indptr, int batch, int max_depth, int topk,
                               int32_t *node_token, int32_t *parent, int32_t *depth,
                               unsigned int *err, cudaStream_t s) {
-    build_tree_kernel<<<batch, 32, 0, s>>>(topk_logp, topk_ids, root_id, budget, qo_indptr,
-                                           max_depth, topk, node_token, parent, depth, err);
-    return cudaGetLastError();
+    return launch_pdl(build_tree_kernel, dim3(batch), dim3(32), 0, s, topk_logp, topk_ids, root_id,
+                      budget, qo_indptr, max_depth, topk, node_token, parent, depth, err);
 }
 
 cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
@@ -305,10 +332,8 @@ cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_i
     const int threads = 256;
     int blocks = (total_words + threads - 1) / threads;
     if (blocks > 4096) blocks = 4096;
-    compile_visibility_kernel<<<blocks, threads, 0, s>>>(parent, qo_indptr, prefix_len,
-                                                         mask_indptr, batch, total_words, mask,
-                                                         err);
-    return cudaGetLastError();
+    return launch_pdl(compile_visibility_kernel, dim3(blocks), dim3(threads), 0, s, parent,
+                      qo_indptr, prefix_len, mask_indptr, batch, total_words, mask, err);
 }
 
 cudaError_t launch_accept(const int32_t *node_token, const int32_t *parent,
@@ -316,9 +341,8 @@ cudaError_t launch_accept(const int32_t *node_token, const int32_t *parent,
                           int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
                           int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
                           cudaStream_t s) {
-    accept_kernel<<<batch, 32, 0, s>>>(node_token, parent, qo_indptr, target_argmax, max_depth,
-                                       accept_len, accepted_nodes, commit_tokens, bonus, err);
-    return cudaGetLastError();
+    return launch_pdl(accept_kernel, dim3(batch), dim3(32), 0, s, node_token, parent, qo_indptr,
+                      target_argmax, max_depth, accept_len, accepted_nodes, commit_tokens, bonus, err);
 }
 
 }  // namespace ddt
