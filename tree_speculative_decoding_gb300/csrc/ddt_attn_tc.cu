@@ -70,12 +70,13 @@ constexpr int kXBytes = (kNb / 4) * 64 * 16;
 constexpr int kOffStage = 0;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;  // two P buffers
 constexpr int kOffX = kOffP + 2 * kPBytes;                // two partial buffers
-constexpr int kOffAlpha = kOffX + 2 * kXBytes;            // 2 x 64 floats
+constexpr int kOffQr = kOffX + 2 * kXBytes;               // Q rope half: 128 rows x 64 B, 64-byte swizzle
+constexpr int kOffAlpha = kOffQr + kRows * 64;             // 2 x 64 floats
 constexpr int kOffLinv = kOffAlpha + 2 * 64 * 4;          // 64 floats
 constexpr int kOffBar = kOffLinv + 64 * 4;
 // barrier slots
 enum {
-    B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL = B_EMPTY0 + kStages, B_SFREE,
+    B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL0 = B_EMPTY0 + kStages, B_SFULL1, B_SFREE0, B_SFREE1,
     B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
     B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
 };
@@ -87,8 +88,8 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;    // 256: output, latent half
-constexpr uint32_t kColQ = 256;  // 144: Q half (128 latent + 16 rope), bf16 pairs
-constexpr uint32_t kColS = 400;  // 64: partial scores
+constexpr uint32_t kColQ = 256;  // 128: Q latent half, bf16 pairs (the rope half is in shared memory)
+constexpr uint32_t kColS = 384;  // 2 x 64: partial scores, double-buffered
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -103,7 +104,7 @@ constexpr uint32_t kIdescS = idesc_bf16(kRows, kNb, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kColS + kNb <= kTmemCols, "tensor memory budget");
+static_assert(kColS + 2 * kNb <= kTmemCols, "tensor memory budget");
 static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 
 struct TcParams {
@@ -192,7 +193,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t count = 1;  // stage empties, score full, PV done: one MMA commit
             if (i < B_EMPTY0) count = 64;                       // stage full: 64 producer lanes
-            else if (i == B_SFREE || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
+            else if (i == B_SFREE0 || i == B_SFREE1 || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
             else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
             else if (i == B_FIN) count = 2;
             mbar_init(bar(i), count);
@@ -215,10 +216,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     // drain, which measured ~700-950 cycles per score block on the part.  The
     // score columns are therefore cleared by the warps that read them, and O
     // once at the start.
-    auto zero_scores = [&]() {
+    auto zero_scores = [&](int sb) {
         const uint32_t z[32] = {};
 #pragma unroll
-        for (int q = 0; q < kNb / 32; ++q) tmem_st32(tmem + lane_off + kColS + 32 * q, z);
+        for (int q = 0; q < kNb / 32; ++q) tmem_st32(tmem + lane_off + kColS + kNb * sb + 32 * q, z);
         tmem_wait_st();
     };
     if (warp < 4) {
@@ -237,15 +238,18 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             }
             tmem_st32(tmem + lane_off + kColQ + 32 * part, w);
         }
-        for (int v = 0; v < 8; ++v) {  // rope half: 32 dims, then 16 zero columns
-            uint4 x = (valid && v < 4) ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
-            w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {  // rope half: 32 dims as a 64-byte-swizzled K-major row
+            const uint4 x = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + kOffQr + (r >> 3) * 512 + (r & 7) * 64 +
+                                       ((v ^ ((r >> 1) & 3)) << 4)) = x;
         }
-        tmem_st32(tmem + lane_off + kColQ + 128, w);
+        fence_proxy_async_smem();  // read by the tensor core
         const uint32_t z[32] = {};
 #pragma unroll
         for (int q = 0; q < 8; ++q) tmem_st32(tmem + lane_off + kColO + 32 * q, z);
-        zero_scores();
+        zero_scores(0);
+        zero_scores(1);
     }
     // Q / O / S in tensor memory before the first MMA: the softmax warps and the
     // MMA warp meet on a named barrier; the producers start gathering at once.
@@ -309,19 +313,21 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         if (lane == 0) {
             auto issue_s = [&](int j) {
                 const uint32_t stage = sbase + kOffStage + (j % kStages) * kStageBytes;
+                const uint32_t sd = tmem + kColS + kNb * (j & 1);
                 fence_proxy_async_smem();  // stage written by cp.async, read by the tensor core
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims
+                for (int ks = 0; ks < 16; ++ks) {  // latent half: 256 dims, A = Q from tensor memory
                     const uint64_t bd = smem_desc(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-                    mma_ts(tmem + kColS, tmem + kColQ + 8 * ks, bd, kIdescS, 1u);
+                    mma_ts(sd, tmem + kColQ + 8 * ks, bd, kIdescS, 1u);
                 }
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims
+                for (int ks = 0; ks < 2; ++ks) {  // rope half: 32 dims, A = Q rope from shared memory
+                    const uint64_t ad = smem_desc(sbase + kOffQr + 32 * ks, 16, 512, kSwizzle64B);
                     const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + 32 * ks, 16, 512, kSwizzle64B);
-                    mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * ks, bd, kIdescS, 1u);
+                    mma_ss(sd, ad, bd, kIdescS, 1u);
                 }
-                mma_commit(bar(B_SFULL));
+                mma_commit(bar(B_SFULL0 + (j & 1)));
             };
             auto issue_pv = [&](int k) {
                 const int s = k % kStages, pb = k & 1;
@@ -344,7 +350,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 if (*abort_flag) break;
                 bool did = false;
                 if (ns < nblk && mbar_test_wait(bar(B_FULL0 + ns % kStages), (ns / kStages) & 1) &&
-                    (ns == 0 || mbar_test_wait(bar(B_SFREE), (ns - 1) & 1))) {
+                    (ns < 2 || mbar_test_wait(bar(B_SFREE0 + (ns & 1)), ((ns - 2) >> 1) & 1))) {
                     issue_s(ns++);
                     did = true;
                 }
@@ -383,20 +389,20 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         bool mask_ready = false;
 
         // read S_j into registers, clear it, and hand the score buffer back to the MMA warp
-        auto take_scores = [&](float (&sv)[kNb]) {
+        auto take_scores = [&](int j, float (&sv)[kNb]) {
             tc_fence_after();
             uint32_t t32[32];
 #pragma unroll
             for (int q = 0; q < kNb / 32; ++q) {
-                tmem_ld32(tmem + lane_off + kColS + 32 * q, t32);
+                tmem_ld32(tmem + lane_off + kColS + kNb * (j & 1) + 32 * q, t32);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(t32[e]);
             }
-            zero_scores();
+            zero_scores(j & 1);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SFREE));
+            if (lane == 0) mbar_arrive(bar(B_SFREE0 + (j & 1)));
         };
         // O row *= alpha before PV_j (only when a row of this warp rescales, which
         // needs PV_{j-1} finished); then this warp's part of P_j is in place.
@@ -435,14 +441,14 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 // uniform readiness tests (tcgen05.ld below is warp-collective)
                 bool can_send = false;
                 if (nsend < nblk && nsend <= nfin + 2) {
-                    bool t = mbar_test_wait(bar(B_SFULL), nsend & 1) &&
+                    bool t = mbar_test_wait(bar(B_SFULL0 + (nsend & 1)), (nsend >> 1) & 1) &&
                              (nsend < 2 || mbar_test_wait(bar(B_XEMPTY0 + (nsend & 1)), ((nsend - 2) >> 1) & 1));
                     can_send = __shfl_sync(0xffffffffu, t, 0);
                 }
                 if (can_send) {
                     const int j = nsend++;
                     float sv[kNb];
-                    take_scores(sv);
+                    take_scores(j, sv);
                     const uint32_t dst = px_row + (j & 1) * kXBytes;
                     const uint32_t p_xfull = map_to_cta(bar(B_XFULL0 + (j & 1)), peer);
 #pragma unroll
@@ -482,8 +488,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             for (int j = 0; j < nblk && ok; ++j) {
                 const int s = j & 1;
                 float sv[kNb];
-                if (!wait_or_abort(bar(B_SFULL), j & 1, abort_flag, a.err)) { ok = false; break; }
-                take_scores(sv);
+                if (!wait_or_abort(bar(B_SFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                take_scores(j, sv);
                 // owner: partner partial + own partial -> softmax -> P for both CTAs
                 if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + s), 32 * kNb * 4);
                 if (!wait_or_abort(bar(B_XFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
