@@ -54,6 +54,12 @@ attn_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ 
 
 }  // namespace
 
+// same shared-memory carveout as the partial pass it overlaps (see tree_prepare_device)
+cudaError_t attn_combine_prepare_device() {
+    return cudaFuncSetAttribute(attn_combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s) {
     const int64_t rows = (int64_t)a.total_q * a.num_heads;
     if (rows == 0) return cudaSuccess;

@@ -68,6 +68,7 @@ constexpr int kPBytes = kRows * 128;
 constexpr int kXBytes = (kNb / 4) * 64 * 16;
 
 constexpr int kOffStage = 0;
+constexpr int kORowStride = 1040;  // epilogue staging of O rows in the idle stages (16 B of padding)
 constexpr int kOffP = kOffStage + kStages * kStageBytes;  // two P buffers
 constexpr int kOffX = kOffP + 2 * kPBytes;                // two partial buffers
 constexpr int kOffQr = kOffX + 2 * kXBytes;               // Q rope half: 128 rows x 64 B, 64-byte swizzle
@@ -78,7 +79,7 @@ constexpr int kOffBar = kOffLinv + 64 * 4;
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL0 = B_EMPTY0 + kStages, B_SFULL1, B_SFREE0, B_SFREE1,
     B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
-    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_COUNT
+    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_ODONE, B_COUNT
 };
 constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // 2 buffers x 2 owner warps: 4-byte "read" signals
 constexpr int kOffHolder = kOffXsig + 16;
@@ -106,6 +107,7 @@ constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kNb <= kTmemCols, "tensor memory budget");
 static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+static_assert(kRows * kORowStride <= kStages * kStageBytes, "epilogue staging fits in the stages");
 
 struct TcParams {
     AttnArgs a;
@@ -196,6 +198,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             else if (i == B_SFREE0 || i == B_SFREE1 || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
             else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
             else if (i == B_FIN) count = 2;
+            // B_ODONE: the single commit after the last PV
             mbar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -368,6 +371,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     __nanosleep(32);  // leave the issue slot to the softmax warp on this sub-partition
                 }
             }
+            if (np == nblk) mma_commit(bar(B_ODONE));  // O complete (single phase)
         }
         __syncwarp();
     } else {
@@ -585,10 +589,11 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         }
 
         // ---- epilogue: O_c / l into the output (or this split's partial) ----
-        // PV_{nblk-2} may still be running here (P is double-buffered), and a
-        // parity wait only tells apart phases one apart: wait for both in order.
-        if (ok && nblk >= 2 && !wait_or_abort(bar(B_PVDONE), (nblk - 2) & 1, abort_flag, a.err)) ok = false;
-        if (ok && wait_or_abort(bar(B_PVDONE), (nblk - 1) & 1, abort_flag, a.err)) {
+        // A parity wait only tells apart phases one apart, and this point may be
+        // reached before, between or after the last two PV completions (the
+        // owner's own PV_{nblk-1} can finish before its thread gets here); the
+        // MMA warp's single commit after the last PV is unambiguous.
+        if (ok && wait_or_abort(bar(B_ODONE), 0, abort_flag, a.err)) {
             pdl_wait();  // the previous kernel may still read this step's output buffers
             float linv = 0.f;
             float lse_v = -INFINITY;
@@ -617,18 +622,27 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     }
                     o += 256 * rank;
                 }
+                // The row (1 KB of fp32) goes through the idle kv stages and leaves
+                // as one bulk copy: per-thread 16-byte global stores of 128 rows at a
+                // 2 KB stride measured ~5 us per CTA.  The 1040-byte row stride spreads
+                // a warp's 16-byte shared-memory stores over all banks.
+                uint8_t *srow = smem + kOffStage + r * kORowStride;
                 uint32_t t32[32];
 #pragma unroll 1
                 for (int q = 0; q < 8; ++q) {
                     tmem_ld32(tmem + lane_off + kColO + 32 * q, t32);
                     tmem_wait_ld();
-                    if (row_valid) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            reinterpret_cast<float4 *>(o + 32 * q + e)[0] =
-                                make_float4(__uint_as_float(t32[e]) * linv, __uint_as_float(t32[e + 1]) * linv,
-                                            __uint_as_float(t32[e + 2]) * linv, __uint_as_float(t32[e + 3]) * linv);
-                    }
+                    for (int e = 0; e < 8; ++e)
+                        reinterpret_cast<float4 *>(srow)[8 * q + e] =
+                            make_float4(__uint_as_float(t32[4 * e]) * linv, __uint_as_float(t32[4 * e + 1]) * linv,
+                                        __uint_as_float(t32[4 * e + 2]) * linv, __uint_as_float(t32[4 * e + 3]) * linv);
+                }
+                fence_proxy_async_smem();  // the row is read by the bulk copy
+                if (row_valid) {
+                    bulk_store_global(o, smem_u32(srow), 256 * 4);
+                    bulk_commit();
+                    bulk_wait_read_all();  // the staged row must outlive the copy's read
                 }
                 if (owner && row_valid && lp) *lp = lse_v;
             }
@@ -657,6 +671,8 @@ int attn_kv_tile() { return kNb; }
 
 cudaError_t attn_prepare_device() {
     cudaError_t e = attn_simt_prepare_device();
+    if (e == cudaSuccess) e = attn_combine_prepare_device();
+    if (e == cudaSuccess) e = tree_prepare_device();
     if (e != cudaSuccess) return e;
     return attn_tc_prepare_device();
 }

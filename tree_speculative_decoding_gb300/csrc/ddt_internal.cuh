@@ -97,6 +97,9 @@ cudaError_t attn_tc_prepare_device();
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t attn_simt_prepare_device();
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
+cudaError_t attn_combine_prepare_device();
+// shared-memory carveout of the small stages' kernels (they overlap the attention)
+cudaError_t tree_prepare_device();
 
 // kv columns per split must be a multiple of this (the attention kv tile)
 int attn_kv_tile();

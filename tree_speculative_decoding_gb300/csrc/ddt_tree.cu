@@ -315,6 +315,22 @@ accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict_
 
 }  // namespace
 
+// The attention kernel needs the SM's largest shared-memory carveout; a kernel
+// that runs beside it must ask for the same, or the SM it lands on cannot take
+// an attention CTA until it drains (measured: the last cluster of the verify
+// step started ~15 us late).
+cudaError_t tree_prepare_device() {
+    cudaError_t e = cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(compile_visibility_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
 cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
                               const int32_t *root_id, const int32_t *budget,
                               const int32_t *qo_indptr, int batch, int max_depth, int topk,
