@@ -41,14 +41,14 @@ METRIC = "verify-attn TFLOP/s and KV GB/s per step, % of roofline, 1xGB300"
 # this workload, from ncu (profiles/attn_tc_single_p4096_b32_h64.md), valid only for the
 # kernel sources it was taken from: a change to them turns the field back to null.
 PROFILE_TRAFFIC = {
-    "bytes": 7308800 + 22016 + 17347840 + 0,
+    "bytes": 7287808 + 0 + 17348096 + 0,
     "sources": {
         "tree_speculative_decoding_gb300/csrc/ddt_attn_tc.cu":
-            "b3216c5861871b3f465436b8460ec802ee1c7fa6f04c6485e52ee41d256986ed",
+            "de3affbee90c30a66e6cd7a2ab7f58cdd0208535ad885fa878b03053976d5cad",
         "tree_speculative_decoding_gb300/csrc/ddt_attn_combine.cu":
-            "f276828594fc64a5ce3a9878d6c94e4ee6ccd4a2b9d072fd4e61320ef27e84d4",
+            "fff3ea27cac45ef762420de5f243eb3900a1ce7161dbf31b0650e630f15fec3a",
         "tree_speculative_decoding_gb300/csrc/ddt_sm100.cuh":
-            "14789d6e497933ab00d5c228a740828f625e9726a881f78f16b8853c1cf9ec08",
+            "6276c6e2e179276103e1e65b6d8341492d3c3f30b50cb73c5abbd5d4257e4f95",
     },
 }
 
