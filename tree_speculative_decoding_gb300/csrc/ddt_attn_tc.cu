@@ -502,7 +502,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q) {
                         const float4 v = x[64 * q];
-                        sv[4 * q] += v.x; sv[4 * q + 1] += v.y; sv[4 * q + 2] += v.z; sv[4 * q + 3] += v.w;
+                        const float2 a = f2add(make_float2(sv[4 * q], sv[4 * q + 1]), make_float2(v.x, v.y));
+                        const float2 c = f2add(make_float2(sv[4 * q + 2], sv[4 * q + 3]), make_float2(v.z, v.w));
+                        sv[4 * q] = a.x; sv[4 * q + 1] = a.y; sv[4 * q + 2] = c.x; sv[4 * q + 3] = c.y;
                     }
                 }
                 __syncwarp();
@@ -554,15 +556,17 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     m_ref = mb;
                 }
                 uint32_t pw[kNb / 2];
-                float lsum = 0.f;
                 const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;  // all -inf rows give p = 0
+                const float2 scv = make_float2(sc, sc), nmv = make_float2(-mref, -mref);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < kNb; k += 2) {
-                    const float p0 = ex2(fmaf(sv[k], sc, -mref)), p1 = ex2(fmaf(sv[k + 1], sc, -mref));
-                    lsum += p0 + p1;
+                    const float2 t = f2fma(make_float2(sv[k], sv[k + 1]), scv, nmv);
+                    const float p0 = ex2(t.x), p1 = ex2(t.y);
+                    acc = f2add(acc, make_float2(p0, p1));
                     pw[k / 2] = pack_bf16(p0, p1);
                 }
-                l += lsum;
+                l += acc.x + acc.y;
                 // both CTAs' P buffer s must be free (PV_{j-2} done in both)
                 if (j >= 2 && !wait_or_abort(bar(B_PEMPTY0 + s), ((j - 2) >> 1) & 1, abort_flag, a.err)) {
                     ok = false;
