@@ -256,6 +256,18 @@ ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
  */
 ddt_status ddt_get_error(void *stream, uint32_t *device_error);
 
+/*
+ * ddt_selftest_wait_timeout -- exercise the failure path of the bounded device
+ * waits without faulting the GPU.  Launches one 32-thread kernel on `stream`
+ * that waits, with the same bounded mbarrier wait the verify kernels use (but
+ * a limit of `poll_limit` polls, 1 .. 2^24), on a barrier that nothing ever
+ * arrives on.  The wait gives up, the kernel latches DDT_DEVERR_TIMEOUT into
+ * the device error word and exits; ddt_get_error() then reports
+ * DDT_ERR_TIMEOUT and the context stays usable.  Returns DDT_ERR_INVALID_ARG
+ * for a limit out of range, DDT_ERR_CUDA if the launch fails, else DDT_OK.
+ */
+ddt_status ddt_selftest_wait_timeout(uint32_t poll_limit, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

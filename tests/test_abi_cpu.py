@@ -104,3 +104,7 @@ def test_host_argument_checks_launch_nothing(lib):
     # misaligned kv_pool
     a2 = [dummy, ctypes.c_void_p(18), 100, dummy, dummy, dummy, dummy, dummy]
     assert lib.ddt_verify_attn(*a2, 1, 8, 9, 9, 30, 0.1, 0, dummy, None, None, 0, None) == 1
+    # the bounded-wait self test checks its poll limit before touching the device
+    lib.ddt_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    assert lib.ddt_selftest_wait_timeout(0, None) == 1
+    assert lib.ddt_selftest_wait_timeout((1 << 24) + 1, None) == 1

@@ -174,6 +174,20 @@ def test_cuda_graph_capture_and_replay():
     assert torch.equal(st.out, ref_out)
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    # failure detection without a fault: a kernel waits on a barrier nothing
+    # arrives on; its bounded wait gives up, latches the timeout bit and exits
+    from tree_speculative_decoding_gb300 import ddt
+    assert ddt.ddt_get_error() == (0, 0)
+    ddt.ddt_selftest_wait_timeout(1 << 12)
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 6 and bits == 0x100
+    assert ddt.ddt_get_error() == (0, 0)     # cleared
+    # the context still runs a verify step, and correctly
+    _full_check(workloads.preset("tiny_p21_b8_h8"), n_rows=10 ** 9)
+
+
 def test_out_of_range_kv_index_is_latched_not_faulted():
     from tree_speculative_decoding_gb300 import ddt
     from tree_speculative_decoding_gb300.pipeline import VerifyStep

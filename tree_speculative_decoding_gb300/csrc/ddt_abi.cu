@@ -239,6 +239,14 @@ ddt_status ddt_get_error(void *stream, uint32_t *device_error) {
     return (word & DDT_DEVERR_TIMEOUT) ? DDT_ERR_TIMEOUT : DDT_ERR_DEVICE_CHECK;
 }
 
+ddt_status ddt_selftest_wait_timeout(uint32_t poll_limit, void *stream) {
+    if (poll_limit < 1 || poll_limit > (1u << 24)) return DDT_ERR_INVALID_ARG;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_wait_timeout_selftest(poll_limit, st->err, as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace ddt {

@@ -28,23 +28,39 @@ attn_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ 
     pdl_wait();  // the partials come from the partial pass
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
-    float m = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[(int64_t)s * rows + row]);
+    // Online merge over groups of four splits: a group's lse values and partial
+    // rows are loaded together (one memory round trip per group), then folded
+    // into the running max m, weight sum den and weighted sum acc.
+    float m = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
-    if (m != -INFINITY) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float ls = lse_part[(int64_t)s * rows + row];
-            if (ls == -INFINITY) continue;
-            const float w = __expf(ls - m);
-            den += w;
-            const float4 o = reinterpret_cast<const float4 *>(
-                o_part + ((int64_t)s * rows + row) * DDT_DL)[threadIdx.x];
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+    for (int s0 = 0; s0 < num_splits; s0 += 4) {
+        float ls[4];
+        float4 o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int s = s0 + t;
+            ls[t] = (s < num_splits) ? lse_part[(int64_t)s * rows + row] : -INFINITY;
+            o[t] = (s < num_splits)
+                ? reinterpret_cast<const float4 *>(o_part + ((int64_t)s * rows + row) * DDT_DL)[threadIdx.x]
+                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        float mg = m;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) mg = fmaxf(mg, ls[t]);
+        if (mg == -INFINITY) continue;  // nothing visible so far
+        const float c = (m == -INFINITY) ? 0.f : __expf(m - mg);  // rescale of the running sums
+        den *= c;
+        acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (ls[t] == -INFINITY) continue;  // a split that saw no column
+            const float w = __expf(ls[t] - mg);
+            den += w;
+            acc.x += w * o[t].x; acc.y += w * o[t].y; acc.z += w * o[t].z; acc.w += w * o[t].w;
+        }
+        m = mg;
+    }
+    if (m != -INFINITY) {
         const float inv = 1.f / den;
         acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     }

@@ -664,7 +664,25 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     }
 }
 
+// One warp waits on a barrier that expects one arrival nobody makes, with the
+// same bounded wait as the verify kernel; it gives up after `limit` polls.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint32_t limit, unsigned int *err) {
+    __shared__ __align__(8) uint64_t never;
+    const uint32_t bar = smem_u32(&never);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (!mbar_wait(bar, 0, limit) && threadIdx.x == 0) latch(err, DDT_DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint32_t poll_limit, unsigned int *err, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(poll_limit, err);
+    return cudaGetLastError();
+}
 
 cudaError_t attn_tc_prepare_device() {
     return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -101,6 +101,10 @@ cudaError_t attn_combine_prepare_device();
 // shared-memory carveout of the small stages' kernels (they overlap the attention)
 cudaError_t tree_prepare_device();
 
+// A kernel whose bounded mbarrier wait can never succeed: it latches
+// DDT_DEVERR_TIMEOUT and exits (the failure path, exercised without a fault).
+cudaError_t launch_wait_timeout_selftest(uint32_t poll_limit, unsigned int *err, cudaStream_t s);
+
 // kv columns per split must be a multiple of this (the attention kv tile)
 int attn_kv_tile();
 

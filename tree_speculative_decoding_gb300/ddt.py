@@ -48,6 +48,7 @@ def _load():
                                      P, P], i32),
         "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
         "ddt_get_error": ([P, P], i32),
+        "ddt_selftest_wait_timeout": ([ctypes.c_uint32, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -206,3 +207,10 @@ def ddt_get_error(stream=None):
     word = ctypes.c_uint32(0)
     st = lib.ddt_get_error(_stream(stream), ctypes.byref(word))
     return st, word.value
+
+
+def ddt_selftest_wait_timeout(poll_limit=1 << 12, stream=None):
+    """Launch the bounded-wait failure check: a kernel waiting on a barrier
+    nobody arrives on gives up after `poll_limit` polls and latches the timeout
+    bit (read it with ddt_get_error)."""
+    _check("ddt_selftest_wait_timeout", lib.ddt_selftest_wait_timeout(int(poll_limit), _stream(stream)))
