@@ -53,14 +53,24 @@ PROFILE_TRAFFIC = {
 }
 
 
+def source_digest(rel):
+    """sha256 of a source file's code with comments and whitespace removed, so that
+    an edit to comments alone keeps a profile valid while any code change voids it."""
+    import hashlib
+    import re
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
 def profiled_traffic():
     """The profiled DRAM bytes if the attention sources are unchanged since, else None."""
-    import hashlib
     for rel, digest in PROFILE_TRAFFIC["sources"].items():
         try:
-            with open(os.path.join(ROOT, rel), "rb") as f:
-                if hashlib.sha256(f.read()).hexdigest() != digest:
-                    return None
+            if source_digest(rel) != digest:
+                return None
         except OSError:
             return None
     return PROFILE_TRAFFIC["bytes"]
@@ -379,7 +389,12 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--source-digests", action="store_true",
+                    help="print the digests of the profiled attention sources and exit")
     args = ap.parse_args(argv)
+    if args.source_digests:
+        print(json.dumps({rel: source_digest(rel) for rel in PROFILE_TRAFFIC["sources"]}, indent=1))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))

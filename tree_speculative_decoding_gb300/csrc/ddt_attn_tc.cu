@@ -14,24 +14,29 @@
 //   * A tile is 128 consecutive (node, head) rows of one request, e.g. two
 //     nodes x 64 heads.  A thread-block cluster of two CTAs owns one tile and
 //     one kv split.  CTA c keeps in tensor memory the fp32 output for latent
-//     half c (128 lanes x 256 columns) and its half of Q's 576 dims as bf16
-//     (latent [256c, 256c+256) and rope [512+32c, 512+32c+32): 144 columns);
-//     the rest holds the score block (64 columns).  A full-width output tile
+//     half c (128 lanes x 256 columns), its latent half of Q as bf16 pairs
+//     (128 columns) and two 64-column score blocks; its 32 rope dims of Q
+//     ([512+32c, 512+32c+32)) sit in shared memory.  A full-width output tile
 //     (512 columns) would leave no room for scores, which is why the latent
 //     dimension is split across the pair.
 //   * Per kv block of 64 columns: two producer warps gather this CTA's half of
 //     the 64 kv rows with 16-byte cp.async copies into a 128-byte-swizzled
 //     stage (four stages); the MMA warp computes partial scores over the dim
-//     half (tcgen05.mma, A = Q from tensor memory, M=128, N=64).  The pair
-//     swaps fp32 partials through distributed shared memory: CTA c owns the
-//     softmax of rows [64c, 64c+64).  The owner adds the two partials, applies
-//     the mask, runs the online softmax (max rescale only when it grows by
-//     more than 2^8), writes P (bf16) locally and bulk-copies its rows to the
-//     partner with the rows' rescale factors.  Each CTA then accumulates
-//     O_c += P V_c (tcgen05.mma, M=128, N=256, K=64, V read as an MN-major
-//     operand straight from the gathered stage).  P and the partner-partial
-//     buffer are double-buffered, so the owner writes P_{j+1} while PV_j still
-//     reads P_j and the partner sends partials one block ahead.
+//     half (tcgen05.mma, M=128, N=64: 16 K-steps with A = Q from tensor memory,
+//     2 with A = rope Q from shared memory) into alternate score blocks.  The
+//     pair swaps fp32 partials through distributed shared memory: CTA c owns
+//     the softmax of rows [64c, 64c+64).  The owner adds the two partials,
+//     applies the mask, runs the online softmax (the running max moves only
+//     when a block max exceeds it by more than 2^20), writes P (bf16) locally
+//     and bulk-copies its rows to the partner with the rows' rescale factors.
+//     Each CTA then accumulates O_c += P V_c (tcgen05.mma, M=128, N=256, K=64,
+//     V read as an MN-major operand straight from the gathered stage).  P and
+//     the partner-partial buffer are double-buffered, so the owner writes
+//     P_{j+1} while PV_j still reads P_j and the partner sends partials one
+//     block ahead.
+//   * Epilogue: after the single commit that follows the last PV, the softmax
+//     warps read O out of tensor memory, scale by 1/l, stage the rows in the
+//     idle gather stages and write each 1 KB row with one bulk copy.
 //   * Distributed-shared-memory traffic moves at ~20 B/clk per direction only
 //     when a warp's stores cover contiguous 512-byte runs (scattered 16-byte
 //     pieces measured 8-9 B/clk), hence the chunk-major partial buffer and the
