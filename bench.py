@@ -189,8 +189,8 @@ def run_device(args, rank, world, local_rank):
             st.run(stream=stream)
     torch.cuda.synchronize()
 
-    # kernels launched per step: tree, mask, attention partial (+ combine), accept
-    launches_per_step = 4 + (1 if st.num_splits > 1 else 0)
+    # kernels launched per step: tree + mask (one launch), attention partial (+ combine), accept
+    launches_per_step = st.launches_per_step
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def one_step(ev):

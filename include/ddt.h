@@ -22,6 +22,17 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Launches are
  *     asynchronous on that stream; no entry point synchronises the host except
  *     ddt_get_error().
+ *   - Every kernel is launched with programmatic dependent launch, so it may
+ *     start while the previous kernel on the stream is still running.  A
+ *     kernel waits for that kernel before it reads anything that an earlier
+ *     stage of this ABI writes (tree, mask, split partials) and before its
+ *     first write.  Arguments that only the caller writes (q, kv_pool,
+ *     kv_indices, the indptr arrays, top-k inputs, target_argmax) are read
+ *     before that wait.  Producing them in a kernel that signals early
+ *     completion (cudaTriggerProgrammaticLaunchCompletion) and then calling
+ *     an entry point right after it is therefore unsupported.  An ordinary
+ *     kernel, a copy or an event between the producer and the call is
+ *     enough.
  *   - bf16 tensors are passed as uint16_t bit patterns.
  *   - Arguments checkable on the host are checked before any launch; a failure
  *     returns DDT_ERR_INVALID_ARG / DDT_ERR_UNSUPPORTED / DDT_ERR_WORKSPACE and
@@ -137,6 +148,25 @@ ddt_status ddt_compile_visibility(const int32_t *parent, const int32_t *qo_indpt
                                   const int32_t *prefix_len, const int32_t *mask_indptr,
                                   int32_t batch, int32_t total_words, uint32_t *mask,
                                   void *stream);
+
+/*
+ * ddt_build_tree_visibility -- ddt_build_tree and ddt_compile_visibility in one
+ * launch, with the outputs of both: the same tree (node_token, parent, depth)
+ * and the same mask words, bit for bit.  One CTA per request: one warp builds
+ * the tree while the others write the all-ones prefix words, then the words
+ * holding tree columns are written from the tree.  The arguments are those of
+ * the two calls (qo_indptr, prefix_len and mask_indptr as for
+ * ddt_compile_visibility; `mask` holds mask_indptr[batch] words).  Saving one
+ * launch lets a following ddt_verify_attn start earlier.  Device errors are
+ * those of the two calls; when the tree cannot be built, its outputs are not
+ * written and the mask words that hold tree columns are written as 0.
+ */
+ddt_status ddt_build_tree_visibility(const float *topk_logp, const int32_t *topk_ids,
+                                     const int32_t *root_id, const int32_t *budget,
+                                     const int32_t *qo_indptr, const int32_t *prefix_len,
+                                     const int32_t *mask_indptr, int32_t batch, int32_t max_depth,
+                                     int32_t topk, int32_t *node_token, int32_t *parent,
+                                     int32_t *depth, uint32_t *mask, void *stream);
 
 /*
  * Split-KV sizing.  ddt_verify_attn_num_splits() returns the split count the

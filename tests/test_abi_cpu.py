@@ -92,6 +92,11 @@ def test_host_argument_checks_launch_nothing(lib):
                               None) == 2
     assert lib.ddt_accept(dummy, dummy, dummy, dummy, 1, 0, dummy, dummy, dummy, dummy, None) == 2
     assert lib.ddt_compile_visibility(None, dummy, dummy, dummy, 1, 10, dummy, None) == 1
+    tv = [dummy] * 7
+    assert lib.ddt_build_tree_visibility(*tv, 1, 7, 8, dummy, dummy, dummy, None, None) == 1
+    assert lib.ddt_build_tree_visibility(*tv, 1, 8, 8, dummy, dummy, dummy, dummy, None) == 2
+    assert lib.ddt_build_tree_visibility(*tv, 1, 7, 0, dummy, dummy, dummy, dummy, None) == 2
+    assert lib.ddt_build_tree_visibility(*tv, 0, 7, 8, dummy, dummy, dummy, dummy, None) == 0
     args = [dummy, dummy, 100, dummy, dummy, dummy, dummy, dummy]
     #        B  H   total_q max_q max_kv scale splits
     bad = [(0, 8, 9, 9, 30, 0.1, 0), (1, 8, 9, 9, 5, 0.1, 0), (1, 8, 9, 9, 30, float("nan"), 0),

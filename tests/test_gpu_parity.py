@@ -28,9 +28,10 @@ def _lib():
     oracle.build()
 
 
-def _step(wl, argmax=None, num_splits=0):
+def _step(wl, argmax=None, num_splits=0, fused=True):
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
-    st = VerifyStep(wl, "cuda:0", target_argmax=argmax, num_splits=num_splits)
+    st = VerifyStep(wl, "cuda:0", target_argmax=argmax, num_splits=num_splits,
+                    fused_tree_mask=fused)
     st.run()
     torch.cuda.synchronize()
     st.check_device_errors()
@@ -71,8 +72,8 @@ def _check_attn(st, wl, mask, mip, rows):
     return diff.max() / np.abs(ref).max()
 
 
-def _full_check(wl, n_rows, argmax=None, num_splits=0):
-    st = _step(wl, argmax=argmax, num_splits=num_splits)
+def _full_check(wl, n_rows, argmax=None, num_splits=0, fused=True):
+    st = _step(wl, argmax=argmax, num_splits=num_splits, fused=fused)
     tok, par, dep = _oracle_tree(wl)
     np.testing.assert_array_equal(st.node_token.cpu().numpy(), tok)
     np.testing.assert_array_equal(st.parent.cpu().numpy(), par)
@@ -143,6 +144,23 @@ def test_degenerate_requests_prefix0_budget0_and_max_qlen():
     wl = workloads.make_workload("edge", 4242, 4, 8, [0, 57, 1, 300], [5, 0, 127, 31], 16, 5000,
                                  1.0)
     _full_check(wl, n_rows=10 ** 9)
+
+
+@pytest.mark.parametrize("name", ["tiny_p21_b8_h8", "ragged_bs8_b32_h64", "mixed_bs32_b16or32_h16"])
+def test_separate_tree_and_mask_launches(name):
+    # ddt_build_tree + ddt_compile_visibility as two launches: the same
+    # oracle outputs as the one-launch ddt_build_tree_visibility of the steps above
+    _full_check(workloads.preset(name), n_rows=256, fused=False)
+
+
+def test_fused_tree_mask_degenerate_requests():
+    # both paths on prefix 0, budget 0, a prefix that is a multiple of 32 and
+    # the largest tree, bit for bit against each other and the oracle
+    wl = workloads.make_workload("edge2", 4243, 5, 4, [0, 64, 1, 300, 31], [5, 0, 127, 31, 2], 16,
+                                 5000, 1.0)
+    a, _ = _full_check(wl, n_rows=10 ** 9, fused=True)
+    b, _ = _full_check(wl, n_rows=10 ** 9, fused=False)
+    assert torch.equal(a.mask, b.mask) and torch.equal(a.parent, b.parent)
 
 
 def test_chain_tree_equals_causal_prefill():
@@ -230,3 +248,8 @@ def test_bad_budget_indptr_is_latched():
     torch.cuda.synchronize()
     status, bits = ddt.ddt_get_error()
     assert status == 5 and bits & 0x1
+    st.build_tree_visibility()               # the one-launch tree + mask checks the same
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 5 and bits & 0x1
+    assert ddt.ddt_get_error() == (0, 0)

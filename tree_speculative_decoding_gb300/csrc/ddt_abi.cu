@@ -126,6 +126,27 @@ ddt_status ddt_compile_visibility(const int32_t *parent, const int32_t *qo_indpt
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
 }
 
+ddt_status ddt_build_tree_visibility(const float *topk_logp, const int32_t *topk_ids,
+                                     const int32_t *root_id, const int32_t *budget,
+                                     const int32_t *qo_indptr, const int32_t *prefix_len,
+                                     const int32_t *mask_indptr, int32_t batch, int32_t max_depth,
+                                     int32_t topk, int32_t *node_token, int32_t *parent,
+                                     int32_t *depth, uint32_t *mask, void *stream) {
+    if (!topk_logp || !topk_ids || !root_id || !budget || !qo_indptr || !prefix_len ||
+        !mask_indptr || !node_token || !parent || !depth || !mask || batch < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH || topk < 1 || topk > DDT_MAX_TOPK)
+        return DDT_ERR_UNSUPPORTED;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_build_tree_visibility(topk_logp, topk_ids, root_id, budget,
+                                                      qo_indptr, batch, max_depth, topk, prefix_len,
+                                                      mask_indptr, node_token, parent, depth, mask,
+                                                      st->err, as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max_q_len,
                                    int32_t max_kv_len, int32_t num_sms) {
     if (batch < 1 || num_heads < 1 || max_q_len < 1 || max_kv_len < 1) return 1;

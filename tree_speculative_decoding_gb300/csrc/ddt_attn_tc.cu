@@ -239,19 +239,25 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
             src = reinterpret_cast<const uint4 *>(a.q + grow * DDT_D);
         }
+        // all of the row's loads first (one memory round trip), then the stores
+        uint4 xl[32], xr[4];
+#pragma unroll
+        for (int v = 0; v < 32; ++v) xl[v] = valid ? src[(256 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) xr[v] = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
         for (int part = 0; part < 4; ++part) {  // latent: 4 x 64 dims
+#pragma unroll
             for (int v = 0; v < 8; ++v) {
-                uint4 x = valid ? src[(256 * rank + 64 * part) / 8 + v] : make_uint4(0, 0, 0, 0);
+                const uint4 x = xl[8 * part + v];
                 w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
             }
             tmem_st32(tmem + lane_off + kColQ + 32 * part, w);
         }
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {  // rope half: 32 dims as a 64-byte-swizzled K-major row
-            const uint4 x = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < 4; ++v)  // rope half: 32 dims as a 64-byte-swizzled K-major row
             *reinterpret_cast<uint4 *>(smem + kOffQr + (r >> 3) * 512 + (r & 7) * 64 +
-                                       ((v ^ ((r >> 1) & 3)) << 4)) = x;
-        }
+                                       ((v ^ ((r >> 1) & 3)) << 4)) = xr[v];
         fence_proxy_async_smem();  // read by the tensor core
         const uint32_t z[32] = {};
 #pragma unroll
@@ -282,37 +288,47 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         const int half = (warp == (rank ? 5 : 4)) ? 0 : 1;
         const int sub = lane >> 3, chunk = lane & 7;
         const char *pool = reinterpret_cast<const char *>(a.kv_pool);
-        // slot of this warp's kv row `lane` of block j, loaded one block ahead so
-        // the index fetch overlaps the wait for a free stage
+        // slot of this warp's kv row `lane` of block j.  Each is loaded one
+        // stage ring ahead (slot_ahead[s] holds block j's while stage s gathers
+        // block j - kStages), so the first kStages blocks need one index round
+        // trip between them and later index loads overlap the stage waits.
         auto fetch_slot = [&](int j) {
             return a.kv_indices[kv0 + min(c_begin + j * kNb + 32 * half + lane, c_end - 1)];  // rows past the end reuse a valid one
         };
-        int next_slot = fetch_slot(0);
-        for (int j = 0; j < nblk && !*abort_flag; ++j) {
-            const int s = j % kStages, u = j / kStages;
-            if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) break;
-            const uint32_t stage = sbase + kOffStage + s * kStageBytes;
-            int mine = next_slot;
-            if (mine < 0 || (int64_t)mine >= a.pool_rows) {
-                latch(a.err, DDT_DEVERR_KV_INDEX);
-                mine = 0;
-            }
-            if (j + 1 < nblk) next_slot = fetch_slot(j + 1);
-#pragma unroll 4
-            for (int g = 0; g < 8; ++g) {
-                const int kk = 4 * g + sub;          // row within this warp's 32
-                const int k = 32 * half + kk;        // kv row within the block
-                const int slot = __shfl_sync(0xffffffffu, mine, kk);
-                const char *src = pool + (int64_t)slot * (DDT_D * 2) + chunk * 16;
-                const uint32_t dst = stage + (k >> 3) * 1024 + (k & 7) * 128 + ((chunk ^ (k & 7)) << 4);
+        int slot_ahead[kStages];
 #pragma unroll
-                for (int bx = 0; bx < 4; ++bx)
-                    cp_async_16(dst + bx * kBoxBytes, src + (256 * rank + 64 * bx) * 2);
-                if (chunk < 4)  // rope: this CTA's 32 dims, 64-byte rows
-                    cp_async_16(stage + 4 * kBoxBytes + k * 64 + ((chunk ^ ((k >> 1) & 3)) << 4),
-                                src + (512 + 32 * rank) * 2);
+        for (int s = 0; s < kStages; ++s) slot_ahead[s] = (s < nblk) ? fetch_slot(s) : 0;
+        bool run = true;
+        for (int j0 = 0; run && j0 < nblk; j0 += kStages) {
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                const int j = j0 + s, u = j0 / kStages;
+                if (j >= nblk) break;
+                if (*abort_flag) { run = false; break; }
+                if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) { run = false; break; }
+                const uint32_t stage = sbase + kOffStage + s * kStageBytes;
+                int mine = slot_ahead[s];
+                if (mine < 0 || (int64_t)mine >= a.pool_rows) {
+                    latch(a.err, DDT_DEVERR_KV_INDEX);
+                    mine = 0;
+                }
+                if (j + kStages < nblk) slot_ahead[s] = fetch_slot(j + kStages);
+#pragma unroll 4
+                for (int g = 0; g < 8; ++g) {
+                    const int kk = 4 * g + sub;          // row within this warp's 32
+                    const int k = 32 * half + kk;        // kv row within the block
+                    const int slot = __shfl_sync(0xffffffffu, mine, kk);
+                    const char *src = pool + (int64_t)slot * (DDT_D * 2) + chunk * 16;
+                    const uint32_t dst = stage + (k >> 3) * 1024 + (k & 7) * 128 + ((chunk ^ (k & 7)) << 4);
+#pragma unroll
+                    for (int bx = 0; bx < 4; ++bx)
+                        cp_async_16(dst + bx * kBoxBytes, src + (256 * rank + 64 * bx) * 2);
+                    if (chunk < 4)  // rope: this CTA's 32 dims, 64-byte rows
+                        cp_async_16(stage + 4 * kBoxBytes + k * 64 + ((chunk ^ ((k >> 1) & 3)) << 4),
+                                    src + (512 + 32 * rank) * 2);
+                }
+                cp_async_arrive(bar(B_FULL0 + s));
             }
-            cp_async_arrive(bar(B_FULL0 + s));
         }
     } else if (warp == mma_warp) {
         // ================= MMA issuer =================

@@ -53,6 +53,12 @@ cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
                               int32_t *node_token, int32_t *parent, int32_t *depth,
                               unsigned int *err, cudaStream_t s);
 
+cudaError_t launch_build_tree_visibility(const float *topk_logp, const int32_t *topk_ids,
+                                         const int32_t *root_id, const int32_t *budget,
+                                         const int32_t *qo_indptr, int batch, int max_depth, int topk,
+                                         const int32_t *prefix_len, const int32_t *mask_indptr,
+                                         int32_t *node_token, int32_t *parent, int32_t *depth,
+                                         uint32_t *mask, unsigned int *err, cudaStream_t s);
 cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
                                       const int32_t *prefix_len, const int32_t *mask_indptr,
                                       int batch, int total_words, uint32_t *mask,

@@ -54,23 +54,14 @@ __device__ __forceinline__ int path_rank(uint32_t path, int depth) {  // rank at
 // with the child (or the sibling) and hands the remaining candidate to lane
 // n % 32, which always has a free slot: lane k receives candidates only at pops
 // n = k, k+32, k+64, k+96 (n <= budget <= 127), at most 4 including the seed.
-__global__ void __launch_bounds__(32)
-build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict__ topk_ids,
-                  const int32_t *__restrict__ root_id, const int32_t *__restrict__ budget,
-                  const int32_t *__restrict__ qo_indptr, int max_depth, int K,
-                  int32_t *__restrict__ node_token, int32_t *__restrict__ parent,
-                  int32_t *__restrict__ depth, unsigned int *err) {
-    __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
-    __shared__ int32_t ids[DDT_MAX_DEPTH * DDT_MAX_TOPK];
-    __shared__ int32_t out_tok[DDT_MAX_Q_LEN], out_par[DDT_MAX_Q_LEN], out_dep[DDT_MAX_Q_LEN];
-    const int b = blockIdx.x;
-    const int lane = threadIdx.x;
-    pdl_trigger();
-    // independent loads first, so their latencies overlap (caller inputs: no wait needed)
-    const int base = qo_indptr[b];
-    const int end = qo_indptr[b + 1];
-    const int nb = budget[b];
-    const int rid = root_id[b];
+// Builds request b's tree in shared memory (out_* [0, nb]) with one warp and
+// returns 0, or the DDT_DEVERR_* bit to latch (the outputs are then unset).
+// Reads only caller inputs, so it may run before the kernel's pdl_wait().
+__device__ unsigned tree_warp(const float *__restrict__ topk_logp,
+                              const int32_t *__restrict__ topk_ids, int b, int base, int end,
+                              int nb, int rid, int max_depth, int K, float *lp, int32_t *ids,
+                              int32_t *out_tok, int32_t *out_par, int32_t *out_dep) {
+    const int lane = threadIdx.x & 31;
     const int total = max_depth * K;
     const float *lpb = topk_logp + (size_t)b * total;
     const int32_t *idb = topk_ids + (size_t)b * total;
@@ -84,26 +75,16 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
         const float v = lp[e];
         if ((e % K) > 0 ? !(v <= lp[e - 1]) : (v != v)) sorted_ok = false;  // also rejects NaN
     }
-    if (__any_sync(FULL, !sorted_ok)) {
-        pdl_wait();
-        if (lane == 0) latch(err, DDT_DEVERR_TOPK_ORDER);
-        return;
-    }
-    if (nb < 0 || nb > DDT_MAX_Q_LEN - 1 || end - base != nb + 1) {
-        pdl_wait();
-        if (lane == 0) latch(err, DDT_DEVERR_QO_INDPTR);
-        return;
-    }
+    if (__any_sync(FULL, !sorted_ok)) return DDT_DEVERR_TOPK_ORDER;
+    if (nb < 0 || nb > DDT_MAX_Q_LEN - 1 || end - base != nb + 1) return DDT_DEVERR_QO_INDPTR;
     if (lane == 0) {
         out_tok[0] = rid;
         out_par[0] = -1;
         out_dep[0] = 0;
     }
-
     if (nb == 0) {
-        pdl_wait();
-        if (lane == 0) { node_token[base] = rid; parent[base] = -1; depth[base] = 0; }
-        return;
+        __syncwarp();
+        return 0;
     }
     uint64_t key[SLOTS];
     float pscore[SLOTS];  // score of the candidate's parent (for its next sibling)
@@ -143,11 +124,7 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
     for (int n = 1; n <= nb; ++n) {
         const uint32_t hi = (uint32_t)(best >> 32);
         const uint32_t mhi = __reduce_max_sync(FULL, hi);
-        if (mhi == 0u) {  // frontier empty: budget exceeds the implicit tree
-            pdl_wait();
-            if (lane == 0) latch(err, DDT_DEVERR_EXHAUSTED);
-            return;
-        }
+        if (mhi == 0u) return DDT_DEVERR_EXHAUSTED;  // frontier empty: budget exceeds the implicit tree
         unsigned who = __ballot_sync(FULL, hi == mhi);
         if (__popc(who) > 1) {  // equal scores: the rest of the key decides
             const uint32_t lo = (uint32_t)best;
@@ -191,11 +168,131 @@ build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict
         if (lane == wl || lane == (n & 31)) prepare();
     }
     __syncwarp();
+    return 0;
+}
+
+__global__ void __launch_bounds__(32)
+build_tree_kernel(const float *__restrict__ topk_logp, const int32_t *__restrict__ topk_ids,
+                  const int32_t *__restrict__ root_id, const int32_t *__restrict__ budget,
+                  const int32_t *__restrict__ qo_indptr, int max_depth, int K,
+                  int32_t *__restrict__ node_token, int32_t *__restrict__ parent,
+                  int32_t *__restrict__ depth, unsigned int *err) {
+    __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t ids[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t out_tok[DDT_MAX_Q_LEN], out_par[DDT_MAX_Q_LEN], out_dep[DDT_MAX_Q_LEN];
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x;
+    pdl_trigger();
+    // caller inputs only until the outputs are written: no wait needed before
+    const int base = qo_indptr[b];
+    const int end = qo_indptr[b + 1];
+    const int nb = budget[b];
+    const unsigned e = tree_warp(topk_logp, topk_ids, b, base, end, nb, root_id[b], max_depth, K,
+                                 lp, ids, out_tok, out_par, out_dep);
     pdl_wait();  // the previous kernel may still read the tree buffers
+    if (e) {
+        if (lane == 0) latch(err, e);
+        return;
+    }
     for (int i = lane; i <= nb; i += 32) {
         node_token[base + i] = out_tok[i];
         parent[base + i] = out_par[i];
         depth[base + i] = out_dep[i];
+    }
+}
+
+// Mask word k of row i of a request with prefix P and q_len T: prefix columns
+// [32k, min(32k+32, P)) and the tree columns P + j for node i and its
+// ancestors j (par: the request's parent links).  A broken parent chain
+// latches DDT_DEVERR_PARENT and ends the walk.
+__device__ __forceinline__ uint32_t mask_word(const int32_t *par, int P, int T, int i, int k,
+                                              unsigned int *err) {
+    const int c0 = k * 32;
+    uint32_t bits = 0u;
+    if (c0 < P) {
+        const int n = min(32, P - c0);
+        bits = (n == 32) ? 0xffffffffu : ((1u << n) - 1u);
+    }
+    if (c0 + 32 > P && c0 < P + T) {
+        int j = i, guard = 0;
+        while (j >= 0) {
+            const int c = P + j;
+            if (c >= c0 && c < c0 + 32) bits |= 1u << (c - c0);
+            const int pj = par[j];
+            if (pj >= j || ++guard > DDT_MAX_Q_LEN) {  // parents must precede
+                if (pj >= 0) latch(err, DDT_DEVERR_PARENT);
+                break;
+            }
+            j = pj;
+        }
+    }
+    return bits;
+}
+
+// Tree build and visibility mask in one launch: one CTA per request.  Warp 0
+// builds the tree while warps 1-7 write the all-ones prefix words of the mask
+// (every word whose 32 columns are prefix columns); after a block barrier all
+// eight warps write the remaining words from the tree in shared memory.
+constexpr int kTreeVisThreads = 256;
+__global__ void __launch_bounds__(kTreeVisThreads)
+build_tree_visibility_kernel(const float *__restrict__ topk_logp,
+                             const int32_t *__restrict__ topk_ids,
+                             const int32_t *__restrict__ root_id,
+                             const int32_t *__restrict__ budget,
+                             const int32_t *__restrict__ qo_indptr, int max_depth, int K,
+                             const int32_t *__restrict__ prefix_len,
+                             const int32_t *__restrict__ mask_indptr,
+                             int32_t *__restrict__ node_token, int32_t *__restrict__ parent,
+                             int32_t *__restrict__ depth, uint32_t *__restrict__ mask,
+                             unsigned int *err) {
+    __shared__ float lp[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t ids[DDT_MAX_DEPTH * DDT_MAX_TOPK];
+    __shared__ int32_t out_tok[DDT_MAX_Q_LEN], out_par[DDT_MAX_Q_LEN], out_dep[DDT_MAX_Q_LEN];
+    __shared__ unsigned tree_err;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    pdl_trigger();
+    const int base = qo_indptr[b];
+    const int end = qo_indptr[b + 1];
+    const int T = end - base;
+    const int P = prefix_len[b];
+    const int W = (P + T + 31) >> 5;
+    const int m0 = mask_indptr[b];
+    const bool mask_ok = T >= 1 && T <= DDT_MAX_Q_LEN && P >= 0 && mask_indptr[b + 1] - m0 == T * W;
+    const int full = mask_ok ? (P >> 5) : 0;  // leading all-ones words per row
+    if (tid < 32) {
+        const int nb = budget[b];
+        const unsigned e = tree_warp(topk_logp, topk_ids, b, base, end, nb, root_id[b], max_depth,
+                                     K, lp, ids, out_tok, out_par, out_dep);
+        if (tid == 0) tree_err = e;
+    } else {
+        pdl_wait();  // the previous kernel may still read the mask
+        for (int w = tid - 32; w < T * full; w += kTreeVisThreads - 32) {
+            const int i = w / full;
+            mask[m0 + i * W + (w - i * full)] = 0xffffffffu;
+        }
+    }
+    __syncthreads();
+    if (tid < 32) pdl_wait();  // the previous kernel may still read the tree buffers
+    const unsigned e = tree_err;
+    if (e) {
+        if (tid == 0) latch(err, e);
+    } else {
+        for (int i = tid; i < T; i += kTreeVisThreads) {
+            node_token[base + i] = out_tok[i];
+            parent[base + i] = out_par[i];
+            depth[base + i] = out_dep[i];
+        }
+    }
+    if (!mask_ok) {
+        if (tid == 0) latch(err, DDT_DEVERR_MASK_INDPTR);
+        return;
+    }
+    const int rest = W - full;  // words per row that hold tree columns
+    for (int w = tid; w < T * rest; w += kTreeVisThreads) {
+        const int i = w / rest;
+        const int k = full + (w - i * rest);
+        mask[m0 + i * W + k] = e ? 0u : mask_word(out_par, P, T, i, k, err);
     }
 }
 
@@ -230,63 +327,53 @@ __global__ void compile_visibility_kernel(const int32_t *__restrict__ parent,
         }
         const int local = w - mask_indptr[b];
         const int i = local / W;
-        const int k = local - i * W;
-        const int c0 = k * 32;
-        uint32_t bits = 0u;
-        // prefix columns [c0, min(c0+32, P))
-        if (c0 < P) {
-            const int n = min(32, P - c0);
-            bits = (n == 32) ? 0xffffffffu : ((1u << n) - 1u);
-        }
-        // tree columns: node i and its ancestors
-        if (c0 + 32 > P && c0 < N) {
-            const int32_t *par = parent + qo_indptr[b];
-            int j = i, guard = 0;
-            while (j >= 0) {
-                const int c = P + j;
-                if (c >= c0 && c < c0 + 32) bits |= 1u << (c - c0);
-                const int pj = par[j];
-                if (pj >= j || ++guard > DDT_MAX_Q_LEN) {  // parents must precede
-                    if (pj >= 0) latch(err, DDT_DEVERR_PARENT);
-                    break;
-                }
-                j = pj;
-            }
-        }
+        const uint32_t bits = mask_word(parent + qo_indptr[b], P, T, i, local - i * W, err);
         mask[w] = bits;
     }
 }
 
 // One warp per request: walk from the root into the child carrying the
-// target's argmax; lanes scan the nodes, the lowest matching index wins.
+// target's argmax; lanes scan the nodes, the lowest matching index wins.  The
+// request's argmax row (a caller input) is staged before the wait for the
+// tree, its parents and tokens right after it, so the walk itself touches
+// shared memory only.
 __global__ void __launch_bounds__(32)
 accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict__ parent,
               const int32_t *__restrict__ qo_indptr, const int32_t *__restrict__ target_argmax,
               int max_depth, int32_t *__restrict__ accept_len,
               int32_t *__restrict__ accepted_nodes, int32_t *__restrict__ commit_tokens,
               int32_t *__restrict__ bonus, unsigned int *err) {
+    __shared__ int32_t s_want[DDT_MAX_Q_LEN], s_par[DDT_MAX_Q_LEN], s_tok[DDT_MAX_Q_LEN];
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     pdl_trigger();
-    pdl_wait();  // the tree comes from the tree build
     const int width = max_depth + 1;
     const int base = qo_indptr[b];
     const int T = qo_indptr[b + 1] - base;
-    int32_t *acc = accepted_nodes + (size_t)b * width;
-    int32_t *com = commit_tokens + (size_t)b * width;
-    if (T < 1 || T > DDT_MAX_Q_LEN) {
+    const bool bad = T < 1 || T > DDT_MAX_Q_LEN;
+    if (!bad)
+        for (int i = lane; i < T; i += 32) s_want[i] = target_argmax[base + i];
+    pdl_wait();  // the tree comes from the tree build
+    if (bad) {
         if (lane == 0) latch(err, DDT_DEVERR_QO_INDPTR);
         return;
     }
+    for (int i = lane; i < T; i += 32) {
+        s_par[i] = parent[base + i];
+        s_tok[i] = node_token[base + i];
+    }
+    __syncwarp();
+    int32_t *acc = accepted_nodes + (size_t)b * width;
+    int32_t *com = commit_tokens + (size_t)b * width;
     int cur = 0, n = 1;
-    int path[DDT_MAX_DEPTH + 1];  // lane 0 keeps the accepted nodes
+    int path[DDT_MAX_DEPTH + 1];  // the accepted nodes (the same in every lane)
     path[0] = 0;
     for (;;) {
-        const int want = target_argmax[base + cur];
+        const int want = s_want[cur];
         int found = -1;
         for (int c0 = 1; c0 < T && found < 0; c0 += 32) {
             const int c = c0 + lane;
-            const bool hit = c < T && parent[base + c] == cur && node_token[base + c] == want;
+            const bool hit = c < T && s_par[c] == cur && s_tok[c] == want;
             const unsigned m = __ballot_sync(FULL, hit);
             if (m) found = c0 + __ffs(m) - 1;
         }
@@ -299,7 +386,7 @@ accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict_
         ++n;
         cur = found;
     }
-    const int bon = target_argmax[base + cur];
+    const int bon = s_want[cur];
     if (lane == 0) {
         accept_len[b] = n;
         bonus[b] = bon;
@@ -307,7 +394,7 @@ accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict_
     for (int k = lane; k < width; k += 32) {
         acc[k] = (k < n) ? path[k] : -1;
         int t = -1;
-        if (k < n - 1) t = node_token[base + path[k + 1]];
+        if (k < n - 1) t = s_tok[path[k + 1]];
         else if (k == n - 1) t = bon;
         com[k] = t;
     }
@@ -322,6 +409,9 @@ accept_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict_
 cudaError_t tree_prepare_device() {
     cudaError_t e = cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(build_tree_visibility_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(compile_visibility_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -338,6 +428,17 @@ cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,
                               unsigned int *err, cudaStream_t s) {
     return launch_pdl(build_tree_kernel, dim3(batch), dim3(32), 0, s, topk_logp, topk_ids, root_id,
                       budget, qo_indptr, max_depth, topk, node_token, parent, depth, err);
+}
+
+cudaError_t launch_build_tree_visibility(const float *topk_logp, const int32_t *topk_ids,
+                                         const int32_t *root_id, const int32_t *budget,
+                                         const int32_t *qo_indptr, int batch, int max_depth, int topk,
+                                         const int32_t *prefix_len, const int32_t *mask_indptr,
+                                         int32_t *node_token, int32_t *parent, int32_t *depth,
+                                         uint32_t *mask, unsigned int *err, cudaStream_t s) {
+    return launch_pdl(build_tree_visibility_kernel, dim3(batch), dim3(kTreeVisThreads), 0, s, topk_logp,
+                      topk_ids, root_id, budget, qo_indptr, max_depth, topk, prefix_len, mask_indptr,
+                      node_token, parent, depth, mask, err);
 }
 
 cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,

@@ -40,6 +40,7 @@ def _load():
         "ddt_build_tree": ([P, P, P, P, P, i32, i32, i32, P, P, P, P], i32),
         "ddt_mask_indptr": ([P, P, i32, P], i32),
         "ddt_compile_visibility": ([P, P, P, P, i32, i32, P, P], i32),
+        "ddt_build_tree_visibility": ([P, P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P], i32),
         "ddt_verify_attn_num_splits": ([i32, i32, i32, i32, i32], i32),
         "ddt_verify_attn_workspace_size": ([i32, i32, i32], sz),
         "ddt_verify_attn": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P,
@@ -115,6 +116,23 @@ def ddt_compile_visibility(parent, qo_indptr, prefix_len, mask_indptr, mask, str
     B = prefix_len.numel()
     _check("ddt_compile_visibility", lib.ddt_compile_visibility(
         _p(parent), _p(qo_indptr), _p(prefix_len), _p(mask_indptr), B, mask.numel(), _p(mask),
+        _stream(stream)))
+
+
+def ddt_build_tree_visibility(topk_logp, topk_ids, root_id, budget, qo_indptr, prefix_len,
+                              mask_indptr, node_token, parent, depth, mask, stream=None):
+    """ddt_build_tree and ddt_compile_visibility in one launch (same outputs)."""
+    B, max_depth, K = topk_logp.shape
+    _dev(topk_logp, torch.float32, "topk_logp")
+    for n, t in (("topk_ids", topk_ids), ("root_id", root_id), ("budget", budget),
+                 ("qo_indptr", qo_indptr), ("prefix_len", prefix_len), ("mask_indptr", mask_indptr),
+                 ("node_token", node_token), ("parent", parent), ("depth", depth)):
+        _dev(t, torch.int32, n)
+    if not (mask.is_cuda and mask.dtype in (torch.int32, torch.uint32) and mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous CUDA 32-bit tensor")
+    _check("ddt_build_tree_visibility", lib.ddt_build_tree_visibility(
+        _p(topk_logp), _p(topk_ids), _p(root_id), _p(budget), _p(qo_indptr), _p(prefix_len),
+        _p(mask_indptr), B, max_depth, K, _p(node_token), _p(parent), _p(depth), _p(mask),
         _stream(stream)))
 
 

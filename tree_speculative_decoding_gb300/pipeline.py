@@ -4,8 +4,10 @@
 in order on one stream: ddt_build_tree -> ddt_compile_visibility ->
 ddt_verify_attn -> ddt_accept (the per-iteration data flow of "The Oracle
 Drafter", section "The Engine Interface Design", with the mask and positions
-built on the device instead of the host).  It only allocates and calls the
-binding; all arithmetic runs in libddt.so.
+built on the device instead of the host).  By default the first two run as
+one launch (ddt_build_tree_visibility); ``fused_tree_mask=False`` calls them
+separately.  It only allocates and calls the binding; all arithmetic runs in
+libddt.so.
 """
 from __future__ import annotations
 
@@ -27,8 +29,9 @@ def _bf16(a, device):
 class VerifyStep:
     """Device-resident inputs and outputs of one verify step for a Workload."""
 
-    def __init__(self, wl, device="cuda", target_argmax=None, num_splits=0):
+    def __init__(self, wl, device="cuda", target_argmax=None, num_splits=0, fused_tree_mask=True):
         self.wl = wl
+        self.fused_tree_mask = fused_tree_mask
         self.device = torch.device(device)
         dev = self.device
         self.B, self.H = wl.B, wl.H
@@ -80,6 +83,11 @@ class VerifyStep:
         ddt.ddt_compile_visibility(self.parent, self.qo_indptr, self.prefix_len, self.mask_indptr,
                                    self.mask, stream)
 
+    def build_tree_visibility(self, stream=None):
+        ddt.ddt_build_tree_visibility(self.topk_logp, self.topk_ids, self.root_id, self.budget,
+                                      self.qo_indptr, self.prefix_len, self.mask_indptr,
+                                      self.node_token, self.parent, self.depth, self.mask, stream)
+
     def verify_attn(self, stream=None):
         ddt.ddt_verify_attn(self.q, self.kv_pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
                             self.mask, self.mask_indptr, self.wl.scale, self.out, self.lse,
@@ -91,9 +99,18 @@ class VerifyStep:
                        self.wl.max_depth, self.accept_len, self.accepted_nodes,
                        self.commit_tokens, self.bonus, stream)
 
+    @property
+    def launches_per_step(self):
+        """Kernels one run() launches: tree (+ mask), mask, attention (+ combine), accept."""
+        attn = 2 if self.num_splits > 1 else 1
+        return (1 if self.fused_tree_mask else 2) + attn + 1
+
     def run(self, stream=None):
-        self.build_tree(stream)
-        self.compile_visibility(stream)
+        if self.fused_tree_mask:
+            self.build_tree_visibility(stream)
+        else:
+            self.build_tree(stream)
+            self.compile_visibility(stream)
         self.verify_attn(stream)
         self.accept(stream)
 
