@@ -388,9 +388,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     *abort_flag = 1;
                     latch(a.err, DDT_DEVERR_TIMEOUT);
                     break;
-                } else {
-                    __nanosleep(32);  // leave the issue slot to the softmax warp on this sub-partition
-                }
+                }  // busy polling measured faster than a nanosleep backoff
             }
             if (np == nblk) mma_commit(bar(B_ODONE));  // O complete (single phase)
         }
@@ -505,8 +503,6 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     *abort_flag = 1;
                     latch(a.err, DDT_DEVERR_TIMEOUT);
                     ok = false;
-                } else {
-                    __nanosleep(32);
                 }
             }
         } else {
