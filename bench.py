@@ -41,14 +41,14 @@ METRIC = "verify-attn TFLOP/s and KV GB/s per step, % of roofline, 1xGB300"
 # this workload, from ncu (profiles/attn_tc_single_p4096_b32_h64.md), valid only for the
 # kernel sources it was taken from: a change to them turns the field back to null.
 PROFILE_TRAFFIC = {
-    "bytes": 7287808 + 0 + 17348096 + 0,
+    "bytes": 7291904 + 0 + 17346560 + 0,
     "sources": {
         "tree_speculative_decoding_gb300/csrc/ddt_attn_tc.cu":
-            "de3affbee90c30a66e6cd7a2ab7f58cdd0208535ad885fa878b03053976d5cad",
+            "e338569085aa0bdedea98eaa2f1b58f17d3e9cd2302851a13108edcdd8cc8a3d",
         "tree_speculative_decoding_gb300/csrc/ddt_attn_combine.cu":
-            "fff3ea27cac45ef762420de5f243eb3900a1ce7161dbf31b0650e630f15fec3a",
+            "fdca4d973e73b3ae2f8c739a639b1e174297c9d7950436970856c620e376355a",
         "tree_speculative_decoding_gb300/csrc/ddt_sm100.cuh":
-            "6276c6e2e179276103e1e65b6d8341492d3c3f30b50cb73c5abbd5d4257e4f95",
+            "13a1fb0bebbc7fa2bd9c7aff8ceb478fb5a3724a59ff051a8a754c7cb8db78ca",
     },
 }
 
