@@ -54,10 +54,11 @@ def _load():
             lib.oracle_verify_attn.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, dbl,
                                                P, i64, P, P, i32]
             lib.oracle_accept.argtypes = [P, P, P, P, i32, i32, P, P, P, P]
+            lib.oracle_commit_kv.argtypes = [P, i64, P, P, P, P, P, i32, i32, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_build_tree, lib.oracle_mask_indptr,
                       lib.oracle_compile_visibility, lib.oracle_verify_attn,
-                      lib.oracle_accept, lib.oracle_num_threads):
+                      lib.oracle_accept, lib.oracle_commit_kv, lib.oracle_num_threads):
                 f.restype = ctypes.c_int
             _lib = lib
         return _lib
@@ -176,6 +177,28 @@ def accept(node_token, parent, qo_indptr, target_argmax, max_depth):
     if rc != 0:
         raise OracleError(f"oracle_accept failed ({rc})")
     return alen, acc, com, bon
+
+
+def commit_kv(kv_pool, kv_indices, kv_indptr, qo_indptr, accept_len, accepted_nodes, max_depth):
+    """KV commit: returns (new pool, new_len).  kv_pool is uint16 (bf16 bits)
+    [pool_rows, 576] and is not modified; the returned copy holds, at
+    positions P_b .. P_b + accept_len - 1 of each request, the accepted
+    nodes' latents in path order."""
+    lib = _load()
+    pool = np.array(kv_pool, dtype=np.uint16, copy=True, order="C")
+    kv_indices = _c(kv_indices, np.int32)
+    kv_indptr = _c(kv_indptr, np.int32)
+    qo_indptr = _c(qo_indptr, np.int32)
+    accept_len = _c(accept_len, np.int32)
+    accepted_nodes = _c(accepted_nodes, np.int32)
+    B = qo_indptr.shape[0] - 1
+    new_len = np.empty(B, np.int32)
+    rc = lib.oracle_commit_kv(_ptr(pool), int(pool.shape[0]), _ptr(kv_indices), _ptr(kv_indptr),
+                              _ptr(qo_indptr), _ptr(accept_len), _ptr(accepted_nodes), B,
+                              int(max_depth), _ptr(new_len))
+    if rc != 0:
+        raise OracleError(f"oracle_commit_kv failed ({rc})")
+    return pool, new_len
 
 
 def best_child_argmax(parent, qo_indptr, node_token, coin, fallback):

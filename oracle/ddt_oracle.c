@@ -34,6 +34,12 @@
  *   [ACC]   "The Oracle Drafter", section "The Engine Interface Design" --
  *           accept produces the accepted path, its length, the commit tokens
  *           and the bonus token.
+ *   [COMMIT] "The Architecture of a Speculative Decoding Engine", the
+ *           append-then-compact scheme and "The Final Resolution: A Concrete
+ *           Trace" -- every tree node's latent is appended after the
+ *           committed prefix; after acceptance only the accepted nodes'
+ *           latents are gathered into contiguous positions and the cache
+ *           grows by accept_len.
  *
  * Readings taken where the pages are silent (each also listed in the design
  * notes):
@@ -359,6 +365,50 @@ int oracle_accept(const int32_t *node_token, const int32_t *parent,
         com[n - 1] = bonus[b];
     }
     return OR_OK;
+}
+
+/*
+ * [COMMIT] Gather the accepted latents of request b into positions
+ * P_b .. P_b + accept_len - 1 of its sequence (position c lives in pool row
+ * kv_indices[kv_indptr[b] + c]).  All source rows are copied out first, then
+ * written, so the result is "the accepted nodes' original latents in path
+ * order" whatever the overlap between sources and destinations.  new_len[b]
+ * = P_b + accept_len[b].  Returns OR_ERR_ARG (and changes nothing for that
+ * request) if the accepted path is not 0 = a_0 < a_1 < ... < q_len or a row
+ * is outside the pool.
+ */
+int oracle_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv_indices,
+                     const int32_t *kv_indptr, const int32_t *qo_indptr,
+                     const int32_t *accept_len, const int32_t *accepted_nodes, int B,
+                     int max_depth, int32_t *new_len) {
+    const int D = 576;
+    int width = max_depth + 1;
+    int status = OR_OK;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)width * D);
+    if (!tmp) return OR_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int T = qo_indptr[b + 1] - qo_indptr[b];
+        int N = kv_indptr[b + 1] - kv_indptr[b];
+        int P = N - T;
+        int n = accept_len[b];
+        const int32_t *acc = accepted_nodes + (size_t)b * width;
+        const int32_t *idx = kv_indices + kv_indptr[b];
+        int ok = n >= 1 && n <= width && n <= T && acc[0] == 0;
+        for (int k = 1; ok && k < n; ++k)
+            if (acc[k] <= acc[k - 1] || acc[k] >= T) ok = 0;
+        for (int k = 0; ok && k < n; ++k) {
+            int64_t src = idx[P + acc[k]], dst = idx[P + k];
+            if (src < 0 || src >= pool_rows || dst < 0 || dst >= pool_rows) ok = 0;
+        }
+        if (!ok) { status = OR_ERR_ARG; continue; }
+        for (int k = 0; k < n; ++k)
+            memcpy(tmp + (size_t)k * D, kv_pool + (size_t)idx[P + acc[k]] * D, sizeof(uint16_t) * D);
+        for (int k = 0; k < n; ++k)
+            memcpy(kv_pool + (size_t)idx[P + k] * D, tmp + (size_t)k * D, sizeof(uint16_t) * D);
+        if (new_len) new_len[b] = P + n;
+    }
+    free(tmp);
+    return status;
 }
 
 int oracle_num_threads(void) {
