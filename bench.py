@@ -266,6 +266,7 @@ def run_device(args, rank, world, local_rank):
             dist.destroy_process_group()
         return None
 
+    commit_ms = time_commit(st, stream, flush)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     ms_per_step = elapsed_max * 1e3 / args.steps
     value = flops_all / elapsed_max / 1e12
@@ -286,7 +287,7 @@ def run_device(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; N(0,1) bf16 q and latent KV; drafter top-k from "
                 "log-softmax of N(0,3) logits)",
-        "config": {"workload": WORKLOAD, "batch": wl.B, "heads": wl.H, "prefix": int(wl.prefix_len[0]),
+        "config": {"workload": wl.name, "batch": wl.B, "heads": wl.H, "prefix": int(wl.prefix_len[0]),
                    "budget": int(wl.budget[0]), "q_len": int(wl.q_len[0]), "topk": wl.K,
                    "pool_rows": wl.pool_rows, "num_splits": st.num_splits,
                    "l2": "flushed (256 MiB write) before every timed step",
@@ -307,6 +308,9 @@ def run_device(args, rank, world, local_rank):
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "commit_kv": {"ms": round(commit_ms, 5), "timing": "ddt_commit_kv alone after the step, each "
+                      "request committing its deepest root-to-leaf path; graph replay, L2 flushed, "
+                      "median"},
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -314,6 +318,47 @@ def run_device(args, rank, world, local_rank):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def time_commit(st, stream, flush, reps=200):
+    """Median time of ddt_commit_kv alone (the step after accept), every request
+    committing the root-to-leaf path of its deepest node (lowest index among the
+    deepest), so that up to max_depth rows move per request."""
+    import torch
+    qo = st.qo_indptr.cpu().numpy()
+    par = st.parent.cpu().numpy()
+    dep = st.depth.cpu().numpy()
+    W = st.wl.max_depth + 1
+    acc = np.full((st.B, W), -1, np.int32)
+    alen = np.zeros(st.B, np.int32)
+    for b in range(st.B):
+        lo, hi = int(qo[b]), int(qo[b + 1])
+        node = int(np.argmax(dep[lo:hi]))
+        path = [node]
+        while path[-1] != 0:
+            path.append(int(par[lo + path[-1]]))
+        path.reverse()
+        alen[b] = len(path)
+        acc[b, :len(path)] = path
+    st.accept_len.copy_(torch.from_numpy(alen))
+    st.accepted_nodes.copy_(torch.from_numpy(acc))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            st.commit_kv(stream=stream)
+    ts = []
+    for i in range(reps + 5):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            ts.append(a.elapsed_time(e))
+    st.check_device_errors()
+    return statistics.median(ts)
 
 
 def oracle_step(wl, rows=None):

@@ -13,6 +13,7 @@
  *   ddt_compile_visibility  bit-packed [q_len, prefix + q_len] visibility mask
  *   ddt_verify_attn         tree-verify MLA attention in absorbed form
  *   ddt_accept              greedy walk: longest accepted chain + bonus token
+ *   ddt_commit_kv           gather the accepted latents after the committed prefix
  *
  * Conventions for every entry point:
  *   - Pointers marked (device) must be device memory of the current CUDA
@@ -86,6 +87,7 @@ typedef enum {
 #define DDT_DEVERR_PARENT       0x040u  /* a parent link that is not an earlier node */
 #define DDT_DEVERR_DEPTH        0x080u  /* accepted chain longer than max_depth + 1 */
 #define DDT_DEVERR_TIMEOUT      0x100u  /* a bounded wait inside a kernel ran out */
+#define DDT_DEVERR_ACCEPTED     0x200u  /* accept_len / accepted_nodes not an accepted path */
 
 const char *ddt_status_string(ddt_status s);
 int32_t ddt_abi_version(void);
@@ -278,6 +280,42 @@ ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
                       int32_t *commit_tokens, int32_t *bonus, void *stream);
 
 /*
+ * ddt_commit_kv -- KV commit after acceptance (compaction of the accepted
+ * latents).
+ * Page: "The Architecture of a Speculative Decoding Engine", sections "The
+ * Final Resolution: A Concrete Trace" and the compaction scheme before it:
+ * the step appended every tree node's latent after the committed prefix
+ * (node j at position P_b + j, the root at P_b); after acceptance the
+ * accepted nodes' latents are gathered into contiguous positions
+ * P_b .. P_b + accept_len - 1, the cache grows by accept_len, and the bonus
+ * token becomes the next step's root at position P_b + accept_len.
+ *
+ * With the slot layout of ddt_verify_attn (position c of request b lives in
+ * pool row kv_indices[kv_indptr[b] + c]), for k = 0 .. accept_len[b]-1:
+ *   row(P_b + k) <- row(P_b + accepted_nodes[b][k])   (all 576 entries)
+ * where every source row is read before any destination row is written, so
+ * a destination that is also a later source (node 2 -> position 1 while
+ * node 5 -> position 2) moves the original latent.  No other pool row is
+ * written.
+ *
+ *   kv_pool       (device) bf16 [pool_rows][576], updated in place.
+ *   kv_indices, kv_indptr, qo_indptr
+ *                 (device) as for ddt_verify_attn (P_b = kv_len_b - q_len_b).
+ *   accept_len, accepted_nodes
+ *                 (device) as written by ddt_accept (max_depth+1 entries per request).
+ *   new_len       (device) int32 [batch] or NULL: P_b + accept_len[b], the
+ *                 committed cache length.
+ * Device checks: accept_len in [1, min(q_len, max_depth+1)], accepted_nodes
+ * starting at 0, strictly increasing and below q_len (DDT_DEVERR_ACCEPTED);
+ * pool rows in range (DDT_DEVERR_KV_INDEX).  A request that fails a check is
+ * left unchanged.
+ */
+ddt_status ddt_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv_indices,
+                         const int32_t *kv_indptr, const int32_t *qo_indptr,
+                         const int32_t *accept_len, const int32_t *accepted_nodes, int32_t batch,
+                         int32_t max_depth, int32_t *new_len, void *stream);
+
+/*
  * ddt_get_error -- read and clear the current device's error word.
  * Synchronises `stream`, copies the word to *device_error (host; may be NULL)
  * and resets it.  Returns DDT_OK when the word was 0, DDT_ERR_TIMEOUT when the
@@ -285,6 +323,83 @@ ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
  * when the copy failed.
  */
 ddt_status ddt_get_error(void *stream, uint32_t *device_error);
+
+/*
+ * ddt_verify_step -- one verify step in one call: ddt_build_tree_visibility,
+ * ddt_verify_attn, ddt_accept and, when `commit_kv` is set, ddt_commit_kv,
+ * launched in that order on `stream`.  It is the whole per-iteration data flow
+ * of "The Oracle Drafter" (section "The Engine Interface Design"), with every
+ * stage on the GPU so that the step can be captured and replayed as one CUDA
+ * graph ("The DDTree CUDA Graph Fix ...", section "Implications and the Path
+ * Forward": graphs were the largest single gain on the pages).
+ *
+ * Each field has the meaning, layout and ownership it has in the call that
+ * consumes it; `total_mask_words` = mask_indptr[batch] is the size of `mask`.
+ * Returns the first non-OK status of the four calls; nothing after that call
+ * is launched.
+ */
+typedef struct {
+    /* tree inputs */
+    const float *topk_logp;
+    const int32_t *topk_ids;
+    const int32_t *root_id;
+    const int32_t *budget;
+    int32_t max_depth;
+    int32_t topk;
+    /* layout: batch, indptrs and host-side bounds */
+    int32_t batch;
+    int32_t total_q;
+    int32_t max_q_len;
+    int32_t max_kv_len;
+    int32_t total_mask_words;
+    const int32_t *qo_indptr;
+    const int32_t *kv_indptr;
+    const int32_t *prefix_len;
+    const int32_t *mask_indptr;
+    /* attention inputs */
+    const uint16_t *q;
+    uint16_t *kv_pool; /* read by the attention, written by the commit */
+    int64_t pool_rows;
+    const int32_t *kv_indices;
+    int32_t num_heads;
+    float scale;
+    int32_t num_splits; /* 0: the library's choice */
+    void *workspace;
+    size_t workspace_bytes;
+    /* accept input */
+    const int32_t *target_argmax;
+    /* outputs */
+    int32_t *node_token;
+    int32_t *parent;
+    int32_t *depth;
+    uint32_t *mask;
+    float *out;
+    float *lse; /* may be NULL */
+    int32_t *accept_len;
+    int32_t *accepted_nodes;
+    int32_t *commit_tokens;
+    int32_t *bonus;
+    /* KV commit: skipped when commit_kv is 0 */
+    int32_t commit_kv;
+    int32_t *new_len; /* may be NULL */
+} ddt_step_args;
+
+ddt_status ddt_verify_step(const ddt_step_args *args, void *stream);
+
+/*
+ * A CUDA graph of one ddt_verify_step, owned by the library: create captures
+ * the step's launches once (the buffers in `args` must then stay allocated and
+ * keep their sizes: the verify buffers are sized for budget+1 tokens per
+ * request, "The DDTree CUDA Graph Fix ...", section "The CUDA Graph Crash: A
+ * Tale of Two Token Counts"); launch replays them on `stream`; destroy frees
+ * the graph.
+ * Create makes no launch of its own; it returns the status of the captured
+ * ddt_verify_step, or DDT_ERR_CUDA if capture or instantiation fails.
+ */
+typedef struct ddt_step_graph ddt_step_graph;
+ddt_status ddt_step_graph_create(const ddt_step_args *args, ddt_step_graph **graph);
+ddt_status ddt_step_graph_launch(ddt_step_graph *graph, void *stream);
+ddt_status ddt_step_graph_destroy(ddt_step_graph *graph);
 
 /*
  * ddt_selftest_wait_timeout -- exercise the failure path of the bounded device

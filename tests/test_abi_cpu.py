@@ -92,6 +92,16 @@ def test_host_argument_checks_launch_nothing(lib):
                               None) == 2
     assert lib.ddt_accept(dummy, dummy, dummy, dummy, 1, 0, dummy, dummy, dummy, dummy, None) == 2
     assert lib.ddt_compile_visibility(None, dummy, dummy, dummy, 1, 10, dummy, None) == 1
+    assert lib.ddt_commit_kv(None, 10, dummy, dummy, dummy, dummy, dummy, 1, 7, None, None) == 1
+    assert lib.ddt_commit_kv(ctypes.c_void_p(24), 10, dummy, dummy, dummy, dummy, dummy, 1, 7,
+                             None, None) == 1  # pool not 16-byte aligned
+    assert lib.ddt_commit_kv(dummy, 0, dummy, dummy, dummy, dummy, dummy, 1, 7, None, None) == 1
+    assert lib.ddt_commit_kv(dummy, 10, dummy, dummy, dummy, dummy, dummy, 1, 8, None, None) == 2
+    assert lib.ddt_commit_kv(dummy, 10, dummy, dummy, dummy, dummy, dummy, 0, 7, None, None) == 0
+    assert lib.ddt_verify_step(None, None) == 1
+    assert lib.ddt_step_graph_create(None, None) == 1
+    assert lib.ddt_step_graph_launch(None, None) == 1
+    assert lib.ddt_step_graph_destroy(None) == 1
     tv = [dummy] * 7
     assert lib.ddt_build_tree_visibility(*tv, 1, 7, 8, dummy, dummy, dummy, None, None) == 1
     assert lib.ddt_build_tree_visibility(*tv, 1, 8, 8, dummy, dummy, dummy, dummy, None) == 2
@@ -113,3 +123,22 @@ def test_host_argument_checks_launch_nothing(lib):
     lib.ddt_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
     assert lib.ddt_selftest_wait_timeout(0, None) == 1
     assert lib.ddt_selftest_wait_timeout((1 << 24) + 1, None) == 1
+
+
+def test_step_args_layout_matches_the_header(tmp_path):
+    # the ctypes mirror of ddt_step_args must agree with the C compiler's layout
+    import subprocess
+    from tree_speculative_decoding_gb300 import ddt
+    fields = [f[0] for f in ddt.StepArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ddt.h"\nint main(void) {\n'
+                   '    printf("%zu\\n", sizeof(ddt_step_args));\n'
+                   + "".join(f'    printf("%zu\\n", offsetof(ddt_step_args, {f}));\n' for f in fields)
+                   + "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(os.path.dirname(__file__), "..", "include"),
+                    "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(ddt.StepArgs)
+    assert got[1:] == [getattr(ddt.StepArgs, f).offset for f in fields]

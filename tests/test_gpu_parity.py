@@ -163,6 +163,137 @@ def test_fused_tree_mask_degenerate_requests():
     assert torch.equal(a.mask, b.mask) and torch.equal(a.parent, b.parent)
 
 
+def _chain_forcing(wl, coin=None):
+    tok, par, _ = _oracle_tree(wl)
+    coin = np.ones(wl.total_q, bool) if coin is None else coin
+    return oracle.best_child_argmax(par, wl.qo_indptr, tok, coin, wl.argmax_random)
+
+
+def _commit_and_check(wl, argmax, full_pool):
+    """Runs the step and the KV commit; checks the pool bit for bit."""
+    st, _ = _full_check(wl, n_rows=64, argmax=argmax)
+    alen = st.accept_len.cpu().numpy()
+    acc = st.accepted_nodes.cpu().numpy()
+    assert alen.max() > 1
+    before = st.kv_pool.clone()
+    st.commit_kv()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    np.testing.assert_array_equal(st.new_len.cpu().numpy(), wl.prefix_len + alen)
+    after = st.kv_pool.view(torch.int16)
+    if full_pool:
+        ref, ref_len = oracle.commit_kv(wl.kv_pool, wl.kv_indices, wl.kv_indptr, wl.qo_indptr,
+                                        alen, acc, wl.max_depth)
+        np.testing.assert_array_equal(after.cpu().numpy().view(np.uint16), ref)
+        return
+    # full size: each destination row holds its source's value from before the
+    # commit, and no other row changed
+    b16 = before.view(torch.int16)
+    dst_all = []
+    for b in range(wl.B):
+        idx = wl.kv_indices[int(wl.kv_indptr[b]):int(wl.kv_indptr[b + 1])]
+        P = int(wl.prefix_len[b])
+        for k in range(int(alen[b])):
+            d, src = int(idx[P + k]), int(idx[P + int(acc[b, k])])
+            assert torch.equal(after[d], b16[src])
+            dst_all.append(d)
+    changed = (after != b16).any(dim=1).nonzero().flatten().cpu().numpy()
+    assert set(changed.tolist()) <= set(dst_all)
+
+
+@pytest.mark.parametrize("name", ["tiny_p21_b8_h8", "edge"])
+def test_commit_kv_matches_oracle(name):
+    if name == "edge":
+        wl = workloads.make_workload("edge_commit", 4244, 5, 4, [0, 64, 1, 300, 31],
+                                     [5, 0, 127, 31, 2], 16, 5000, 1.0)
+    else:
+        wl = workloads.preset(name)
+    _commit_and_check(wl, _chain_forcing(wl), full_pool=True)
+    # half-matching targets: paths stop at random depths
+    coin = np.random.default_rng(7).random(wl.total_q) < 0.6
+    coin[wl.qo_indptr[:-1]] = True
+    _commit_and_check(wl, _chain_forcing(wl, coin), full_pool=True)
+
+
+@pytest.mark.parametrize("name", ["single_p4096_b32_h64", "mixed_bs32_b16or32_h16"])
+def test_commit_kv_full_size(name):
+    wl = workloads.preset(name)
+    _commit_and_check(wl, _chain_forcing(wl), full_pool=False)
+
+
+def test_commit_kv_rejects_a_broken_path():
+    from tree_speculative_decoding_gb300 import ddt
+    wl = workloads.preset("tiny_p21_b8_h8")
+    st = _step(wl, argmax=_chain_forcing(wl))
+    before = st.kv_pool.clone()
+    st.accepted_nodes[0, 1] = 0          # not increasing: made on the host, caught by the kernel
+    st.commit_kv()
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status == 5 and bits & 0x200
+    assert torch.equal(st.kv_pool, before)
+
+
+def _outputs(st):
+    return [t.clone() for t in (st.node_token, st.parent, st.depth, st.mask, st.out, st.lse,
+                                 st.accept_len, st.accepted_nodes, st.commit_tokens, st.bonus)]
+
+
+@pytest.mark.parametrize("name", ["tiny_p21_b8_h8", "single_p4096_b32_h64", "edge"])
+def test_one_call_step_and_step_graph_equal_the_staged_calls(name):
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    if name == "edge":
+        wl = workloads.make_workload("edge_step", 4245, 5, 4, [0, 64, 1, 300, 31],
+                                     [5, 0, 127, 31, 2], 16, 5000, 1.0)
+    else:
+        wl = workloads.preset(name)
+    st, _ = _full_check(wl, n_rows=64)             # staged calls, checked against the oracle
+    ref = _outputs(st)
+    st2 = VerifyStep(wl, "cuda:0")
+    st2.run_one_call()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    for a, b in zip(ref, _outputs(st2)):
+        assert torch.equal(a, b)
+    for t in (st2.node_token, st2.out, st2.accept_len):
+        t.zero_()
+    g = st2.step_graph()                           # captured once, replayed three times
+    for _ in range(3):
+        g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    for a, b in zip(ref, _outputs(st2)):
+        assert torch.equal(a, b)
+    g.close()
+
+
+def test_step_graph_with_commit_equals_the_staged_commit():
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.preset("tiny_p21_b8_h8")
+    am = _chain_forcing(wl)
+    st = _step(wl, argmax=am)
+    st.commit_kv()
+    torch.cuda.synchronize()
+    st2 = VerifyStep(wl, "cuda:0", target_argmax=am)
+    g = st2.step_graph(commit_kv=True)
+    g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    assert torch.equal(st.kv_pool, st2.kv_pool) and torch.equal(st.new_len, st2.new_len)
+    assert st.accept_len.max().item() > 1
+
+
+def test_step_graph_reports_a_host_check_and_makes_no_graph():
+    from tree_speculative_decoding_gb300 import ddt
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    st = VerifyStep(workloads.preset("tiny_p21_b8_h8"), "cuda:0")
+    a = st.step_args()
+    a.max_depth = 8                                # unsupported: refused before any launch
+    with pytest.raises(ddt.DDTError) as e:
+        ddt.StepGraph(a)
+    assert e.value.status == 2
+
+
 def test_chain_tree_equals_causal_prefill():
     wl = workloads.make_workload("chain", 77, 1, 4, [40], [7], 1, 300, 2.0)
     st, (tok, par, dep) = _full_check(wl, n_rows=10 ** 9)

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "ddt_internal.cuh"
 
@@ -246,6 +247,23 @@ ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
 }
 
+ddt_status ddt_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv_indices,
+                         const int32_t *kv_indptr, const int32_t *qo_indptr,
+                         const int32_t *accept_len, const int32_t *accepted_nodes, int32_t batch,
+                         int32_t max_depth, int32_t *new_len, void *stream) {
+    if (!kv_pool || !kv_indices || !kv_indptr || !qo_indptr || !accept_len || !accepted_nodes ||
+        batch < 0 || pool_rows < 1 || (reinterpret_cast<uintptr_t>(kv_pool) & 15u))
+        return DDT_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH) return DDT_ERR_UNSUPPORTED;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_commit_kv(kv_pool, pool_rows, kv_indices, kv_indptr, qo_indptr,
+                                          accept_len, accepted_nodes, batch, max_depth, new_len,
+                                          st->err, as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 ddt_status ddt_get_error(void *stream, uint32_t *device_error) {
     DeviceState *st = device_state();
     if (!st) return DDT_ERR_CUDA;
@@ -268,6 +286,76 @@ ddt_status ddt_selftest_wait_timeout(uint32_t poll_limit, void *stream) {
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- one-call step
+
+ddt_status ddt_verify_step(const ddt_step_args *a, void *stream) {
+    if (!a) return DDT_ERR_INVALID_ARG;
+    ddt_status st = ddt_build_tree_visibility(a->topk_logp, a->topk_ids, a->root_id, a->budget,
+                                              a->qo_indptr, a->prefix_len, a->mask_indptr,
+                                              a->batch, a->max_depth, a->topk, a->node_token,
+                                              a->parent, a->depth, a->mask, stream);
+    if (st != DDT_OK) return st;
+    st = ddt_verify_attn(a->q, a->kv_pool, a->pool_rows, a->kv_indices, a->kv_indptr,
+                         a->qo_indptr, a->mask, a->mask_indptr, a->batch, a->num_heads,
+                         a->total_q, a->max_q_len, a->max_kv_len, a->scale, a->num_splits,
+                         a->out, a->lse, a->workspace, a->workspace_bytes, stream);
+    if (st != DDT_OK) return st;
+    st = ddt_accept(a->node_token, a->parent, a->qo_indptr, a->target_argmax, a->batch,
+                    a->max_depth, a->accept_len, a->accepted_nodes, a->commit_tokens, a->bonus,
+                    stream);
+    if (st != DDT_OK || !a->commit_kv) return st;
+    return ddt_commit_kv(a->kv_pool, a->pool_rows, a->kv_indices, a->kv_indptr, a->qo_indptr,
+                         a->accept_len, a->accepted_nodes, a->batch, a->max_depth, a->new_len,
+                         stream);
+}
+
+struct ddt_step_graph {
+    cudaGraphExec_t exec = nullptr;
+};
+
+ddt_status ddt_step_graph_create(const ddt_step_args *a, ddt_step_graph **graph) {
+    if (!a || !graph) return DDT_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (!device_state()) return DDT_ERR_CUDA;  // one-time set-up outside the capture
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DDT_ERR_CUDA;
+    ddt_status st = DDT_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        st = ddt_verify_step(a, s);
+        const cudaError_t e = cudaStreamEndCapture(s, &g);  // ends the capture on every path
+        if (st == DDT_OK && e != cudaSuccess) st = DDT_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (st == DDT_OK && cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) st = DDT_ERR_CUDA;
+    if (g) cudaGraphDestroy(g);
+    cudaStreamDestroy(s);
+    if (st != DDT_OK) {
+        if (exec) cudaGraphExecDestroy(exec);
+        return st;
+    }
+    ddt_step_graph *h = new (std::nothrow) ddt_step_graph;
+    if (!h) {
+        cudaGraphExecDestroy(exec);
+        return DDT_ERR_CUDA;
+    }
+    h->exec = exec;
+    *graph = h;
+    return DDT_OK;
+}
+
+ddt_status ddt_step_graph_launch(ddt_step_graph *graph, void *stream) {
+    if (!graph || !graph->exec) return DDT_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, as_stream(stream)) == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+ddt_status ddt_step_graph_destroy(ddt_step_graph *graph) {
+    if (!graph) return DDT_ERR_INVALID_ARG;
+    const cudaError_t e = graph->exec ? cudaGraphExecDestroy(graph->exec) : cudaSuccess;
+    delete graph;
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace ddt {
@@ -278,3 +366,4 @@ unsigned int *device_error_word() {
     return st ? st->err : nullptr;
 }
 }  // namespace ddt
+

@@ -100,10 +100,13 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;
 // Lazy rescale: the running max m (log2 units) moves only when a block's max
-// exceeds it by more than this, so p = 2^(s - m) <= 2^20 -- far inside bf16 and
-// fp32 range -- while a rescale of O (a serial 256-column TMEM read-modify-
-// write, ~0.7 us) stays rare.
-constexpr float kRescaleLog2 = 20.0f;
+// exceeds it by more than this, so p = 2^(s - m) <= 2^48.  P (bf16) and the
+// fp32 sums keep their relative precision at any scale; the sums stay finite
+// while N * 2^48 * max|v| < 2^128, i.e. for |v| below ~2^59 at a million kv
+// columns.  A rescale of O (a serial 256-column TMEM read-modify-write after
+// waiting for the previous PV) costs ~1-2 us, so it should stay rare: with 1%
+// of kv rows scaled by 8, a threshold of 20 measured 1.3% slower.
+constexpr float kRescaleLog2 = 48.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kIdescS = idesc_bf16(kRows, kNb, 0, 0);
@@ -712,6 +715,7 @@ cudaError_t attn_prepare_device() {
     cudaError_t e = attn_simt_prepare_device();
     if (e == cudaSuccess) e = attn_combine_prepare_device();
     if (e == cudaSuccess) e = tree_prepare_device();
+    if (e == cudaSuccess) e = commit_prepare_device();
     if (e != cudaSuccess) return e;
     return attn_tc_prepare_device();
 }

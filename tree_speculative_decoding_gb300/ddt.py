@@ -48,8 +48,13 @@ def _load():
         "ddt_verify_attn_noalloc": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P,
                                      P, P], i32),
         "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
+        "ddt_commit_kv": ([P, i64, P, P, P, P, P, i32, i32, P, P], i32),
         "ddt_get_error": ([P, P], i32),
         "ddt_selftest_wait_timeout": ([ctypes.c_uint32, P], i32),
+        "ddt_verify_step": ([P, P], i32),
+        "ddt_step_graph_create": ([P, P], i32),
+        "ddt_step_graph_launch": ([P, P], i32),
+        "ddt_step_graph_destroy": ([P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -59,6 +64,25 @@ def _load():
 
 
 lib = _load()
+
+
+class StepArgs(ctypes.Structure):
+    """ddt_step_args of include/ddt.h, field for field."""
+    _P, _i32 = ctypes.c_void_p, ctypes.c_int32
+    _fields_ = [
+        ("topk_logp", _P), ("topk_ids", _P), ("root_id", _P), ("budget", _P),
+        ("max_depth", _i32), ("topk", _i32),
+        ("batch", _i32), ("total_q", _i32), ("max_q_len", _i32), ("max_kv_len", _i32),
+        ("total_mask_words", _i32),
+        ("qo_indptr", _P), ("kv_indptr", _P), ("prefix_len", _P), ("mask_indptr", _P),
+        ("q", _P), ("kv_pool", _P), ("pool_rows", ctypes.c_int64), ("kv_indices", _P),
+        ("num_heads", _i32), ("scale", ctypes.c_float), ("num_splits", _i32),
+        ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
+        ("target_argmax", _P),
+        ("node_token", _P), ("parent", _P), ("depth", _P), ("mask", _P), ("out", _P), ("lse", _P),
+        ("accept_len", _P), ("accepted_nodes", _P), ("commit_tokens", _P), ("bonus", _P),
+        ("commit_kv", _i32), ("new_len", _P),
+    ]
 
 
 def _p(t):
@@ -218,6 +242,52 @@ def ddt_accept(node_token, parent, qo_indptr, target_argmax, max_depth, accept_l
     _check("ddt_accept", lib.ddt_accept(
         _p(node_token), _p(parent), _p(qo_indptr), _p(target_argmax), B, int(max_depth),
         _p(accept_len), _p(accepted_nodes), _p(commit_tokens), _p(bonus), _stream(stream)))
+
+
+def ddt_commit_kv(kv_pool, kv_indices, kv_indptr, qo_indptr, accept_len, accepted_nodes, max_depth,
+                  new_len=None, stream=None):
+    """KV commit: gathers each request's accepted latents into positions
+    P .. P + accept_len - 1 of its sequence, in place in kv_pool."""
+    _dev(kv_pool, torch.bfloat16, "kv_pool")
+    for n, t in (("kv_indices", kv_indices), ("kv_indptr", kv_indptr), ("qo_indptr", qo_indptr),
+                 ("accept_len", accept_len), ("accepted_nodes", accepted_nodes)):
+        _dev(t, torch.int32, n)
+    if new_len is not None:
+        _dev(new_len, torch.int32, "new_len")
+    B = qo_indptr.numel() - 1
+    _check("ddt_commit_kv", lib.ddt_commit_kv(
+        _p(kv_pool), kv_pool.shape[0], _p(kv_indices), _p(kv_indptr), _p(qo_indptr),
+        _p(accept_len), _p(accepted_nodes), B, int(max_depth), _p(new_len), _stream(stream)))
+
+
+def ddt_verify_step(args: StepArgs, stream=None):
+    """One verify step in one call (tree + mask, attention, accept, optional commit)."""
+    _check("ddt_verify_step", lib.ddt_verify_step(ctypes.byref(args), _stream(stream)))
+
+
+class StepGraph:
+    """A library-owned CUDA graph of one ddt_verify_step; the tensors behind
+    `args` must outlive it."""
+
+    def __init__(self, args: StepArgs, keep_alive=()):
+        self._keep = (args, tuple(keep_alive))
+        h = ctypes.c_void_p()
+        _check("ddt_step_graph_create", lib.ddt_step_graph_create(ctypes.byref(args), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check("ddt_step_graph_launch", lib.ddt_step_graph_launch(self._h, _stream(stream)))
+
+    def close(self):
+        if self._h:
+            _check("ddt_step_graph_destroy", lib.ddt_step_graph_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def ddt_get_error(stream=None):

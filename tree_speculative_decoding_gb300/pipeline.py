@@ -68,6 +68,7 @@ class VerifyStep:
         self.accepted_nodes = torch.empty((self.B, W), dtype=torch.int32, device=dev)
         self.commit_tokens = torch.empty((self.B, W), dtype=torch.int32, device=dev)
         self.bonus = torch.empty(self.B, dtype=torch.int32, device=dev)
+        self.new_len = torch.empty(self.B, dtype=torch.int32, device=dev)
 
         self.num_splits = num_splits or ddt.ddt_verify_attn_num_splits(
             self.B, self.H, self.max_q_len, self.max_kv_len)
@@ -98,6 +99,45 @@ class VerifyStep:
         ddt.ddt_accept(self.node_token, self.parent, self.qo_indptr, self.target_argmax,
                        self.wl.max_depth, self.accept_len, self.accepted_nodes,
                        self.commit_tokens, self.bonus, stream)
+
+    def commit_kv(self, stream=None):
+        """The step after accept: the accepted latents move to the positions after
+        the prefix, in place in kv_pool; new_len = prefix + accept_len."""
+        ddt.ddt_commit_kv(self.kv_pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
+                          self.accept_len, self.accepted_nodes, self.wl.max_depth, self.new_len,
+                          stream)
+
+    def step_args(self, commit_kv=False):
+        """The step's buffers as one ddt_step_args (for ddt_verify_step and StepGraph)."""
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        a = ddt.StepArgs()
+        a.topk_logp, a.topk_ids, a.root_id, a.budget = (p(self.topk_logp), p(self.topk_ids),
+                                                        p(self.root_id), p(self.budget))
+        a.max_depth, a.topk = self.wl.max_depth, self.wl.K
+        a.batch, a.total_q, a.max_q_len, a.max_kv_len = self.B, self.total_q, self.max_q_len, self.max_kv_len
+        a.total_mask_words = self.total_words
+        a.qo_indptr, a.kv_indptr = p(self.qo_indptr), p(self.kv_indptr)
+        a.prefix_len, a.mask_indptr = p(self.prefix_len), p(self.mask_indptr)
+        a.q, a.kv_pool, a.pool_rows, a.kv_indices = (p(self.q), p(self.kv_pool), self.kv_pool.shape[0],
+                                                     p(self.kv_indices))
+        a.num_heads, a.scale, a.num_splits = self.H, self.wl.scale, self.num_splits
+        a.workspace = p(self.workspace)
+        a.workspace_bytes = 0 if self.workspace is None else self.workspace.numel()
+        a.target_argmax = p(self.target_argmax)
+        a.node_token, a.parent, a.depth, a.mask = p(self.node_token), p(self.parent), p(self.depth), p(self.mask)
+        a.out, a.lse = p(self.out), p(self.lse)
+        a.accept_len, a.accepted_nodes = p(self.accept_len), p(self.accepted_nodes)
+        a.commit_tokens, a.bonus = p(self.commit_tokens), p(self.bonus)
+        a.commit_kv, a.new_len = int(bool(commit_kv)), p(self.new_len)
+        return a
+
+    def run_one_call(self, stream=None, commit_kv=False):
+        """The step as a single C call (ddt_verify_step)."""
+        ddt.ddt_verify_step(self.step_args(commit_kv), stream)
+
+    def step_graph(self, commit_kv=False):
+        """A library-owned CUDA graph of the step (ddt_step_graph_*)."""
+        return ddt.StepGraph(self.step_args(commit_kv), keep_alive=(self,))
 
     @property
     def launches_per_step(self):
