@@ -720,15 +720,31 @@ cudaError_t attn_prepare_device() {
     return attn_tc_prepare_device();
 }
 
+// Split count from host-side bounds only (no per-request lengths): the grid
+// runs in waves of num_sms / 2 clusters, and a cluster costs its kv blocks plus
+// a fixed fill / epilogue share worth ~8 blocks.  The count minimising
+// waves x (blocks per split + 8) wins, the smallest on ties, with at least 4
+// blocks per split.  Measured on the part, this picks the best count of those
+// tried for one request (4 at prefix 4096, 2 at prefix 131072), for a ragged
+// batch of 8 (1) and for a mixed batch of 32 (3; 2 and 3 tie, 1 is 16% slower).
 int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
     const long long tiles = (long long)batch * (((long long)max_q_len * num_heads + kRows - 1) / kRows);
-    const long long pairs = num_sms / 2;
-    long long splits = pairs / tiles;
-    const long long by_len = max_kv_len / (4 * kNb);  // keep >= 4 blocks per split
-    if (splits > by_len) splits = by_len;
-    if (splits < 1) splits = 1;
-    if (splits > DDT_MAX_SPLITS) splits = DDT_MAX_SPLITS;
-    return (int)splits;
+    const long long pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    const long long blocks = ((long long)max_kv_len + kNb - 1) / kNb;
+    long long smax = blocks / 4;  // keep >= 4 blocks per split
+    if (smax > DDT_MAX_SPLITS) smax = DDT_MAX_SPLITS;
+    if (smax < 1) smax = 1;
+    constexpr long long kFixedBlocks = 8;
+    long long best = 1, best_cost = -1;
+    for (long long sp = 1; sp <= smax; ++sp) {
+        const long long waves = (tiles * sp + pairs - 1) / pairs;
+        const long long cost = waves * ((blocks + sp - 1) / sp + kFixedBlocks);
+        if (best_cost < 0 || cost < best_cost) {
+            best = sp;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 
 cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
