@@ -236,14 +236,13 @@ def run_device(args, rank, world, local_rank):
     elapsed = sum(step_ms) / 1e3
     elapsed_max, flops_all = reduce_over_ranks(elapsed, flops * args.steps, dist)
 
-    # end to end through host buffers: per-step inputs from pinned memory, the
-    # same graph, then the results back to pinned memory
-    h_in = {name: getattr(st, name).detach().cpu().pin_memory()
-            for name in ("topk_logp", "topk_ids", "root_id", "kv_indices", "q", "target_argmax")}
-    h_out = {name: torch.empty_like(getattr(st, name), device="cpu").pin_memory()
-             for name in ("out", "lse", "accept_len", "commit_tokens", "bonus")}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    # end to end through host buffers: the step's inputs (one packed buffer) from
+    # pinned host memory, the same graph, then the step's results (one packed
+    # buffer) back to pinned host memory -- one copy each way
+    h_in = st.inputs.buf.cpu().pin_memory()
+    h_out = torch.empty_like(st.outputs.buf, device="cpu").pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
     e2e_steps = max(10, args.steps // 10)
     e2e_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
               for _ in range(e2e_steps)]
@@ -251,11 +250,9 @@ def run_device(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             flush.zero_()
             e2e_ev[i][0].record(stream)
-            for name, t in h_in.items():
-                getattr(st, name).copy_(t, non_blocking=True)
+            st.inputs.buf.copy_(h_in, non_blocking=True)
             graph.replay()
-            for name, t in h_out.items():
-                t.copy_(getattr(st, name), non_blocking=True)
+            h_out.copy_(st.outputs.buf, non_blocking=True)
             e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)

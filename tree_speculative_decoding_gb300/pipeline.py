@@ -26,6 +26,31 @@ def _bf16(a, device):
         torch.bfloat16).to(device)
 
 
+class _Arena:
+    """One contiguous device buffer holding several tensors at 256-byte-aligned
+    offsets.  Each entry is (name, dtype, data or shape): numpy data (uint16
+    holding bf16 bits for bfloat16) is copied in, a shape is left uninitialised."""
+
+    def __init__(self, entries, device):
+        layout, off = [], 0
+        for name, dtype, src in entries:
+            shape = tuple(src) if isinstance(src, tuple) else tuple(np.shape(src))
+            nbytes = int(np.prod(shape, dtype=np.int64)) * torch.empty((), dtype=dtype).element_size()
+            layout.append((name, dtype, shape, off, nbytes, None if isinstance(src, tuple) else src))
+            off += (nbytes + 255) // 256 * 256
+        self.buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.views = {}
+        for name, dtype, shape, o, nbytes, src in layout:
+            v = self.buf[o:o + nbytes].view(dtype).view(shape)
+            if src is not None:
+                if dtype == torch.bfloat16:
+                    host = torch.from_numpy(np.ascontiguousarray(src, np.uint16).view(np.int16)).view(torch.bfloat16)
+                else:
+                    host = torch.from_numpy(np.ascontiguousarray(src)).to(dtype)
+                v.copy_(host.reshape(shape))
+            self.views[name] = v
+
+
 class VerifyStep:
     """Device-resident inputs and outputs of one verify step for a Workload."""
 
@@ -38,37 +63,36 @@ class VerifyStep:
         self.total_q = wl.total_q
         self.max_q_len = int(wl.q_len.max())
         self.max_kv_len = int(wl.kv_len.max())
-        self.topk_logp = torch.from_numpy(np.ascontiguousarray(wl.topk_logp)).to(dev)
-        self.topk_ids = _i32(wl.topk_ids, dev)
-        self.root_id = _i32(wl.root_id, dev)
-        self.budget = _i32(wl.budget, dev)
-        self.qo_indptr = _i32(wl.qo_indptr, dev)
-        self.kv_indptr = _i32(wl.kv_indptr, dev)
-        self.kv_indices = _i32(wl.kv_indices, dev)
-        self.prefix_len = _i32(wl.prefix_len, dev)
-        self.q = _bf16(wl.q, dev)
-        self.kv_pool = _bf16(wl.kv_pool, dev)
-        argmax = wl.argmax_random if target_argmax is None else target_argmax
-        self.target_argmax = _i32(argmax, dev)
         mip = ddt.ddt_mask_indptr(torch.from_numpy(wl.qo_indptr.astype(np.int32)),
                                   torch.from_numpy(wl.prefix_len.astype(np.int32)))
         self.mask_indptr_host = mip
-        self.mask_indptr = mip.to(dev)
         self.total_words = int(mip[-1])
-
-        T = self.total_q
+        argmax = wl.argmax_random if target_argmax is None else target_argmax
+        T, W = self.total_q, wl.max_depth + 1
+        # Per-step inputs in one device buffer and the step's results in another,
+        # so that a host round trip is one copy each way.
+        self.inputs = _Arena([
+            ("topk_logp", torch.float32, np.ascontiguousarray(wl.topk_logp, np.float32)),
+            ("topk_ids", torch.int32, wl.topk_ids), ("root_id", torch.int32, wl.root_id),
+            ("budget", torch.int32, wl.budget), ("qo_indptr", torch.int32, wl.qo_indptr),
+            ("kv_indptr", torch.int32, wl.kv_indptr), ("kv_indices", torch.int32, wl.kv_indices),
+            ("prefix_len", torch.int32, wl.prefix_len), ("mask_indptr", torch.int32, mip.numpy()),
+            ("target_argmax", torch.int32, argmax),
+            ("q", torch.bfloat16, wl.q)], dev)
+        for name, t in self.inputs.views.items():
+            setattr(self, name, t)
+        self.outputs = _Arena([
+            ("out", torch.float32, (T, self.H, ddt.DL)), ("lse", torch.float32, (T, self.H)),
+            ("accept_len", torch.int32, (self.B,)), ("accepted_nodes", torch.int32, (self.B, W)),
+            ("commit_tokens", torch.int32, (self.B, W)), ("bonus", torch.int32, (self.B,)),
+            ("new_len", torch.int32, (self.B,))], dev)
+        for name, t in self.outputs.views.items():
+            setattr(self, name, t)
+        self.kv_pool = _bf16(wl.kv_pool, dev)  # the resident cache, not a per-step input
         self.node_token = torch.empty(T, dtype=torch.int32, device=dev)
         self.parent = torch.empty(T, dtype=torch.int32, device=dev)
         self.depth = torch.empty(T, dtype=torch.int32, device=dev)
         self.mask = torch.empty(self.total_words, dtype=torch.int32, device=dev)
-        self.out = torch.empty((T, self.H, ddt.DL), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((T, self.H), dtype=torch.float32, device=dev)
-        W = wl.max_depth + 1
-        self.accept_len = torch.empty(self.B, dtype=torch.int32, device=dev)
-        self.accepted_nodes = torch.empty((self.B, W), dtype=torch.int32, device=dev)
-        self.commit_tokens = torch.empty((self.B, W), dtype=torch.int32, device=dev)
-        self.bonus = torch.empty(self.B, dtype=torch.int32, device=dev)
-        self.new_len = torch.empty(self.B, dtype=torch.int32, device=dev)
 
         self.num_splits = num_splits or ddt.ddt_verify_attn_num_splits(
             self.B, self.H, self.max_q_len, self.max_kv_len)
