@@ -99,6 +99,7 @@ constexpr uint32_t kColS = 384;  // 2 x 64: partial scores, double-buffered
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kOrderMaxBatch = 256;  // longest-first dispatch order up to this many requests
 // Lazy rescale: the running max m (log2 units) moves only when a block's max
 // exceeds it by more than this, so p = 2^(s - m) <= 2^48.  P (bf16) and the
 // fp32 sums keep their relative precision at any scale; the sums stay finite
@@ -154,7 +155,26 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const uint32_t peer = rank ^ 1u;
     const int split = blockIdx.x >> 1;
     const int tile = blockIdx.y;
-    const int b = blockIdx.z;
+    // Clusters are dispatched in block-index order, request by request.  With
+    // several requests, blockIdx.z = k takes the request with the k-th most kv
+    // columns (ties by index), so the longest requests start first and a long
+    // one never waits for the last wave.  Every CTA derives the same order from
+    // kv_indptr; the idle stage memory is the scratch.
+    int b = blockIdx.z;
+    if (a.batch > 1 && a.batch <= kOrderMaxBatch) {
+        int *s_len = reinterpret_cast<int *>(smem + kOffStage);
+        int *s_req = s_len + kOrderMaxBatch;
+        for (int i = tid; i < a.batch; i += kThreads) s_len[i] = a.kv_indptr[i + 1] - a.kv_indptr[i];
+        __syncthreads();
+        for (int r = tid; r < a.batch; r += kThreads) {
+            const int len = s_len[r];
+            int k = 0;
+            for (int o = 0; o < a.batch; ++o) k += (s_len[o] > len) || (s_len[o] == len && o < r);
+            if (k == (int)blockIdx.z) *s_req = r;
+        }
+        __syncthreads();
+        b = *s_req;
+    }
 
     // ---- work of this tile / split (identical in both CTAs of the pair) ----
     const int H = a.num_heads;
@@ -720,16 +740,21 @@ cudaError_t attn_prepare_device() {
     return attn_tc_prepare_device();
 }
 
-// Split count from host-side bounds only (no per-request lengths): the grid
-// runs in waves of num_sms / 2 clusters, and a cluster costs its kv blocks plus
-// a fixed fill / epilogue share worth ~8 blocks.  The count minimising
-// waves x (blocks per split + 8) wins, the smallest on ties, with at least 4
-// blocks per split.  Measured on the part, this picks the best count of those
-// tried for one request (4 at prefix 4096, 2 at prefix 131072), for a ragged
-// batch of 8 (1) and for a mixed batch of 32 (3; 2 and 3 tie, 1 is 16% slower).
+// Split count from host-side bounds only (no per-request lengths).  Several
+// requests that already fill a wave of clusters (num_sms / 2 of them) take
+// one split: the kernel starts the longest requests first, which balances the
+// waves better than splitting did (a mixed batch of 32: 209 us with one split,
+// 259-300 us with 2-4; a ragged batch of 8: 329 us against 358-379 us).
+// Otherwise the grid runs in waves of num_sms / 2 clusters, and a cluster
+// costs its kv blocks plus a fixed fill / epilogue share worth ~8 blocks.  The
+// count minimising waves x (blocks per split + 8) wins, the smallest on ties,
+// with at least 4 blocks per split.  For one request this picks the best count
+// measured (4 at prefix 4096, 9 at prefix 131072, where 297 clusters fill four
+// waves almost exactly).
 int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
     const long long tiles = (long long)batch * (((long long)max_q_len * num_heads + kRows - 1) / kRows);
     const long long pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    if (batch > 1 && tiles >= pairs) return 1;
     const long long blocks = ((long long)max_kv_len + kNb - 1) / kNb;
     long long smax = blocks / 4;  // keep >= 4 blocks per split
     if (smax > DDT_MAX_SPLITS) smax = DDT_MAX_SPLITS;
