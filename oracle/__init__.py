@@ -55,10 +55,14 @@ def _load():
                                                P, i64, P, P, i32]
             lib.oracle_accept.argtypes = [P, P, P, P, i32, i32, P, P, P, P]
             lib.oracle_commit_kv.argtypes = [P, i64, P, P, P, P, P, i32, i32, P]
+            lib.oracle_tree_links.argtypes = [P, P, i32, P, P, P]
+            lib.oracle_accept_sampled.argtypes = [P, P, P, P, i32, P, P, P, i32, i32, i32,
+                                                  P, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_build_tree, lib.oracle_mask_indptr,
                       lib.oracle_compile_visibility, lib.oracle_verify_attn,
-                      lib.oracle_accept, lib.oracle_commit_kv, lib.oracle_num_threads):
+                      lib.oracle_accept, lib.oracle_commit_kv, lib.oracle_tree_links,
+                      lib.oracle_accept_sampled, lib.oracle_num_threads):
                 f.restype = ctypes.c_int
             _lib = lib
         return _lib
@@ -199,6 +203,48 @@ def commit_kv(kv_pool, kv_indices, kv_indptr, qo_indptr, accept_len, accepted_no
     if rc != 0:
         raise OracleError(f"oracle_commit_kv failed ({rc})")
     return pool, new_len
+
+
+def tree_links(parent, qo_indptr):
+    """(first_child, next_sibling, retrieve_index) of the tree: local indices,
+    -1 where there is none; retrieve_index is the node's global row."""
+    lib = _load()
+    parent = _c(parent, np.int32)
+    qo_indptr = _c(qo_indptr, np.int32)
+    n = parent.shape[0]
+    fc, ns, ri = (np.empty(n, np.int32) for _ in range(3))
+    rc = lib.oracle_tree_links(_ptr(parent), _ptr(qo_indptr), qo_indptr.shape[0] - 1, _ptr(fc),
+                               _ptr(ns), _ptr(ri))
+    if rc != 0:
+        raise OracleError(f"oracle_tree_links failed ({rc})")
+    return fc, ns, ri
+
+
+def accept_sampled(node_token, parent, qo_indptr, logits, temperature, top_k, coins, max_depth):
+    """Sampling accept (reading R15).  logits float32 [rows, vocab]; temperature
+    float32 [B]; top_k int32 [B]; coins float32 [rows, coin_stride].  Returns
+    (accept_len, accepted_nodes, commit_tokens, bonus) as accept() does."""
+    lib = _load()
+    node_token = _c(node_token, np.int32)
+    parent = _c(parent, np.int32)
+    qo_indptr = _c(qo_indptr, np.int32)
+    logits = _c(logits, np.float32)
+    temperature = _c(temperature, np.float32)
+    top_k = _c(top_k, np.int32)
+    coins = _c(coins, np.float32)
+    B = qo_indptr.shape[0] - 1
+    W = int(max_depth) + 1
+    alen = np.empty(B, np.int32)
+    acc = np.empty((B, W), np.int32)
+    com = np.empty((B, W), np.int32)
+    bon = np.empty(B, np.int32)
+    rc = lib.oracle_accept_sampled(_ptr(node_token), _ptr(parent), _ptr(qo_indptr), _ptr(logits),
+                                   int(logits.shape[1]), _ptr(temperature), _ptr(top_k), _ptr(coins),
+                                   int(coins.shape[1]), B, int(max_depth), _ptr(alen), _ptr(acc),
+                                   _ptr(com), _ptr(bon))
+    if rc != 0:
+        raise OracleError(f"oracle_accept_sampled failed ({rc})")
+    return alen, acc, com, bon
 
 
 def best_child_argmax(parent, qo_indptr, node_token, coin, fallback):

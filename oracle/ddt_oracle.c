@@ -34,6 +34,12 @@
  *   [ACC]   "The Oracle Drafter", section "The Engine Interface Design" --
  *           accept produces the accepted path, its length, the commit tokens
  *           and the bonus token.
+ *   [SAMPLE] "The DDTree CUDA Graph Fix ...", section "Temperature Support:
+ *           Already Working for Linear, Planned for DDTree" -- sampling accept
+ *           reuses a tree rejection-sampling kernel that takes the tree as
+ *           (retrieve_index, retrieve_next_token, retrieve_next_sibling) and
+ *           filters the target with temperature and top-k.  The pages give no
+ *           algorithm text; the reading taken is R15 below.
  *   [COMMIT] "The Architecture of a Speculative Decoding Engine", the
  *           append-then-compact scheme and "The Final Resolution: A Concrete
  *           Trace" -- every tree node's latent is appended after the
@@ -55,6 +61,16 @@
  *       token equals the target's argmax is followed.
  *   R7  a row with no visible column gives out = 0 and lse = -inf.
  *   R8  accept_len counts the root; commit tokens = accepted drafts + bonus.
+ *   R15 sampling accept (target-only, deterministic drafts): at node n the
+ *       target distribution p is softmax(logits[n] / T) over the tokens whose
+ *       logit is at least the top_k-th largest (all of them when top_k <= 0
+ *       or >= vocab; ties kept).  The children of n are tried in index order
+ *       against the residual r (p minus the tokens already rejected): child c
+ *       with token t is taken when coin[n][i] < r(t) / mass(r), else t leaves
+ *       the residual.  With no child taken, the bonus is the first token id v
+ *       whose cumulative residual mass exceeds coin[n][last] * mass(r).  This
+ *       emits every token with probability p, and T <= 0 (p = one-hot at the
+ *       argmax, lowest id on ties) is the greedy walk exactly.
  */
 #include <math.h>
 #include <stdint.h>
@@ -408,6 +424,130 @@ int oracle_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv_ind
         if (new_len) new_len[b] = P + n;
     }
     free(tmp);
+    return status;
+}
+
+/*
+ * [SAMPLE] The tree in the sampling kernel's format: for node n of request b,
+ * retrieve_index[n] = qo_indptr[b] + n (its row), first_child[n] = the lowest
+ * index child of n or -1 (retrieve_next_token), next_sibling[n] = the next
+ * higher index child of n's parent or -1 (retrieve_next_sibling).  Indices
+ * other than retrieve_index are local to the request.
+ */
+int oracle_tree_links(const int32_t *parent, const int32_t *qo_indptr, int B,
+                      int32_t *first_child, int32_t *next_sibling, int32_t *retrieve_index) {
+    for (int b = 0; b < B; ++b) {
+        int base = qo_indptr[b];
+        int T = qo_indptr[b + 1] - base;
+        for (int n = 0; n < T; ++n) {
+            first_child[base + n] = -1;
+            next_sibling[base + n] = -1;
+            retrieve_index[base + n] = base + n;
+        }
+        for (int c = 1; c < T; ++c) {
+            int p = parent[base + c];
+            if (p < 0 || p >= c) return OR_ERR_ARG;
+            if (first_child[base + p] < 0) {
+                first_child[base + p] = c;
+            } else {
+                int s = first_child[base + p];
+                while (next_sibling[base + s] >= 0) s = next_sibling[base + s];
+                next_sibling[base + s] = c;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+static int cmp_desc(const void *a, const void *b) {
+    float x = *(const float *)a, y = *(const float *)b;
+    return (x < y) - (x > y);
+}
+
+/*
+ * [SAMPLE] reading R15.  coins is [rows][coin_stride] uniform [0,1): coin i is
+ * for the i-th child tried at that node, the last one for the bonus draw.
+ * Outputs as in oracle_accept.
+ */
+int oracle_accept_sampled(const int32_t *node_token, const int32_t *parent,
+                          const int32_t *qo_indptr, const float *logits, int vocab,
+                          const float *temperature, const int32_t *top_k, const float *coins,
+                          int coin_stride, int B, int max_depth, int32_t *accept_len,
+                          int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus) {
+    int width = max_depth + 1;
+    double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+    float *sorted = (float *)malloc(sizeof(float) * (size_t)vocab);
+    if (!p || !sorted) { free(p); free(sorted); return OR_ERR_ARG; }
+    int status = OR_OK;
+    for (int b = 0; b < B && status == OR_OK; ++b) {
+        int base = qo_indptr[b];
+        int T = qo_indptr[b + 1] - base;
+        int32_t *acc = accepted_nodes + (size_t)b * width;
+        int32_t *com = commit_tokens + (size_t)b * width;
+        for (int k = 0; k < width; ++k) { acc[k] = -1; com[k] = -1; }
+        int cur = 0, n = 0;
+        acc[n++] = 0;
+        for (;;) {
+            const float *l = logits + (size_t)(base + cur) * vocab;
+            const float *u = coins + (size_t)(base + cur) * coin_stride;
+            /* the target distribution p at this node */
+            int amax = 0;
+            for (int v = 1; v < vocab; ++v) if (l[v] > l[amax]) amax = v;
+            if (temperature[b] <= 0.0f) {
+                for (int v = 0; v < vocab; ++v) p[v] = (v == amax) ? 1.0 : 0.0;
+            } else {
+                float thr = -INFINITY;
+                int k = top_k[b];
+                if (k > 0 && k < vocab) {
+                    memcpy(sorted, l, sizeof(float) * (size_t)vocab);
+                    qsort(sorted, (size_t)vocab, sizeof(float), cmp_desc);
+                    thr = sorted[k - 1];
+                }
+                double z = 0.0;
+                for (int v = 0; v < vocab; ++v) {
+                    p[v] = (l[v] >= thr) ? exp(((double)l[v] - (double)l[amax]) / (double)temperature[b]) : 0.0;
+                    z += p[v];
+                }
+                for (int v = 0; v < vocab; ++v) p[v] /= z;
+            }
+            /* the children, in index order, against the residual */
+            double mass = 1.0;
+            int next = -1, tried = 0;
+            for (int c = 1; c < T; ++c) {
+                if (parent[base + c] != cur) continue;
+                if (tried >= coin_stride - 1) { status = OR_ERR_ARG; break; }
+                int t = node_token[base + c];
+                double pt = (t >= 0 && t < vocab) ? p[t] : 0.0;
+                if ((double)u[tried] < pt / mass) { next = c; break; }
+                if (t >= 0 && t < vocab) { mass -= pt; p[t] = 0.0; }
+                ++tried;
+            }
+            if (status != OR_OK) break;
+            if (next >= 0) {
+                if (n >= width) { status = OR_ERR_ARG; break; }   /* deeper than max_depth */
+                acc[n++] = next;
+                cur = next;
+                continue;
+            }
+            /* bonus: inverse CDF of the residual in token-id order */
+            double target = (double)u[coin_stride - 1] * mass, cum = 0.0;
+            int bon = -1, last = -1;
+            for (int v = 0; v < vocab; ++v) {
+                if (p[v] <= 0.0) continue;
+                last = v;
+                cum += p[v];
+                if (cum > target) { bon = v; break; }
+            }
+            if (bon < 0) bon = (last >= 0) ? last : amax;
+            accept_len[b] = n;
+            bonus[b] = bon;
+            for (int k = 1; k < n; ++k) com[k - 1] = node_token[base + acc[k]];
+            com[n - 1] = bon;
+            break;
+        }
+    }
+    free(p);
+    free(sorted);
     return status;
 }
 

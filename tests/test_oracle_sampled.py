@@ -1,0 +1,143 @@
+"""Pins for the oracle's sampling accept and tree links (CPU only).
+
+"The DDTree CUDA Graph Fix ...", section "Temperature Support: Already Working
+for Linear, Planned for DDTree": sampling accept runs tree rejection sampling
+on the target distribution (temperature, top-k), with the tree given as
+(retrieve_index, retrieve_next_token, retrieve_next_sibling).  The pages give
+no algorithm text, so the reading (R15) is pinned by what any correct reading
+must satisfy:
+- every emitted token is distributed as the target distribution, a Monte Carlo
+  check against a softmax computed here;
+- at temperature 0 it is the greedy walk;
+- a hand-worked example;
+- the links agree with the children sets.
+"""
+import numpy as np
+import pytest
+
+from tests import _brute
+
+
+def _tree(seed, K=3, D=4, budget=25):
+    rng = np.random.default_rng(seed)
+    lp = -np.sort(rng.exponential(1.0, size=(D, K)), axis=1).astype(np.float32)
+    ids = np.stack([rng.choice(40, K, replace=False) for _ in range(D)]).astype(np.int32)
+    return _brute.brute_tree(lp, ids, 9, budget, D, K)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tree_links_follow_the_children_sets(oracle_mod, seed):
+    tok, par, dep, _ = _tree(seed)
+    T = len(tok)
+    qo = np.array([0, T], np.int32)
+    fc, ns, ri = oracle_mod.tree_links(par, qo)
+    children = {n: sorted(c for c in range(1, T) if par[c] == n) for n in range(T)}
+    for n in range(T):
+        assert fc[n] == (children[n][0] if children[n] else -1)
+        sibs = children[par[n]] if n > 0 else [0]
+        later = [c for c in sibs if c > n]
+        assert ns[n] == (later[0] if later else -1)
+    assert ri.tolist() == list(range(T))
+
+
+def test_tree_links_ragged_rows_are_global(oracle_mod):
+    par = np.array([-1, 0, 0, 1, -1, 0], np.int32)
+    fc, ns, ri = oracle_mod.tree_links(par, np.array([0, 4, 6], np.int32))
+    assert fc.tolist() == [1, 3, -1, -1, 1, -1]
+    assert ns.tolist() == [-1, 2, -1, -1, -1, -1]
+    assert ri.tolist() == [0, 1, 2, 3, 4, 5]
+
+
+def _softmax_topk(l, T, k):
+    l = l.astype(np.float64)
+    keep = np.ones_like(l, bool) if k <= 0 or k >= len(l) else l >= np.sort(l)[::-1][k - 1]
+    w = np.where(keep, np.exp((l - l.max()) / T), 0.0)
+    return w / w.sum()
+
+
+def test_hand_worked_example(oracle_mod):
+    # vocab 4, T = 1, logits log([1, 2, 1, 4]) at both nodes: p = [1, 2, 1, 4] / 8.
+    # root (token 7) has children 1 (token 3) and 2 (token 1).
+    #  child 1: a = p(3) / 1 = 0.5, coin 0.6 -> rejected, residual mass 0.5
+    #  child 2: a = p(1) / 0.5 = 0.5, coin 0.3 -> taken
+    # node 2 has no children; bonus coin 0.5: residual p, cumulative
+    #  0.125, 0.375, 0.5, 1.0 first exceeds 0.5 at token 3
+    par = np.array([-1, 0, 0], np.int32)
+    tok = np.array([7, 3, 1], np.int32)
+    logits = np.tile(np.log(np.array([1, 2, 1, 4], np.float32)), (3, 1)).astype(np.float32)
+    coins = np.array([[0.6, 0.3, 0.9], [0.9, 0.9, 0.9], [0.9, 0.9, 0.5]], np.float32)
+    alen, acc, com, bon = oracle_mod.accept_sampled(tok, par, np.array([0, 3], np.int32), logits,
+                                                    np.array([1.0], np.float32),
+                                                    np.array([0], np.int32), coins, 3)
+    assert alen.tolist() == [2]
+    assert acc[0].tolist() == [0, 2, -1, -1]
+    assert com[0].tolist() == [1, 3, -1, -1]
+    assert bon.tolist() == [3]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_temperature_zero_is_the_greedy_walk(oracle_mod, seed):
+    tok, par, dep, _ = _tree(seed)
+    T = len(tok)
+    rng = np.random.default_rng(100 + seed)
+    logits = rng.normal(size=(T, 40)).astype(np.float32)
+    # make the argmax land on a child token often, so that walks go deep
+    for n in range(T):
+        kids = [c for c in range(1, T) if par[c] == n]
+        if kids and rng.random() < 0.7:
+            logits[n, tok[kids[rng.integers(len(kids))]]] = 9.0
+    coins = rng.random((T, 4)).astype(np.float32)
+    qo = np.array([0, T], np.int32)
+    got = oracle_mod.accept_sampled(tok, par, qo, logits, np.array([0.0], np.float32),
+                                    np.array([5], np.int32), coins, 4)
+    ref = oracle_mod.accept(tok, par, qo, logits.argmax(axis=1).astype(np.int32), 4)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+    # top_k = 1 keeps only the argmax token: the same walk at any temperature
+    got1 = oracle_mod.accept_sampled(tok, par, qo, logits, np.array([0.8], np.float32),
+                                     np.array([1], np.int32), coins, 4)
+    for g, r in zip(got1, ref):
+        np.testing.assert_array_equal(g, r)
+
+
+@pytest.mark.parametrize("temp,top_k,kids", [(1.0, 0, [2, 5, 0]), (0.6, 4, [5, 1]), (1.3, 0, [])])
+def test_emitted_tokens_follow_the_target_distribution(oracle_mod, temp, top_k, kids):
+    # one root with children carrying tokens `kids` (each child a leaf); over many
+    # coin draws, the first emitted token must follow p(root), and after taking
+    # a child the second must follow p(child)
+    V, n = 6, 20000
+    rng = np.random.default_rng(7)
+    T = 1 + len(kids)
+    par = np.array([-1] + [0] * len(kids), np.int32)
+    tok = np.array([9] + kids, np.int32)
+    logits = rng.normal(scale=1.5, size=(T, V)).astype(np.float32)
+    # n independent requests sharing the tree, coins drawn per request
+    B = n
+    par_b = np.tile(par, B)
+    tok_b = np.tile(tok, B)
+    logits_b = np.tile(logits, (B, 1))
+    qo_b = np.arange(B + 1, dtype=np.int32) * T
+    coins = rng.random((B * T, 4)).astype(np.float32)
+    alen, acc, com, bon = oracle_mod.accept_sampled(
+        tok_b, par_b, qo_b, logits_b, np.full(B, temp, np.float32), np.full(B, top_k, np.int32),
+        coins, 2)
+    p_root = _softmax_topk(logits[0], temp, top_k)
+    first = com[:, 0]
+    freq = np.bincount(first, minlength=V) / B
+    assert np.abs(freq - p_root).max() < 4.5 * np.sqrt(p_root.max() * (1 - p_root.min()) / B) + 1e-9
+    for ci, t in enumerate(kids):
+        took = first == t
+        if took.sum() < 2000:
+            continue
+        p_child = _softmax_topk(logits[1 + ci], temp, top_k)
+        f2 = np.bincount(com[took, 1], minlength=V) / took.sum()
+        assert np.abs(f2 - p_child).max() < 4.5 * np.sqrt(0.25 / took.sum())
+
+
+def test_more_children_than_coins_is_rejected(oracle_mod):
+    par = np.array([-1, 0, 0, 0], np.int32)
+    tok = np.array([0, 1, 2, 3], np.int32)
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.accept_sampled(tok, par, np.array([0, 4], np.int32),
+                                  np.zeros((4, 5), np.float32), np.array([1.0], np.float32),
+                                  np.array([0], np.int32), np.full((4, 3), 0.99, np.float32), 3)
