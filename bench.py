@@ -264,6 +264,7 @@ def run_device(args, rank, world, local_rank):
         return None
 
     commit_ms = time_commit(st, stream, flush)
+    sampled_ms = time_sampled(st, stream, flush, wl.vocab)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     ms_per_step = elapsed_max * 1e3 / args.steps
     value = flops_all / elapsed_max / 1e12
@@ -305,6 +306,9 @@ def run_device(args, rank, world, local_rank):
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "accept_sampled": {"ms": round(sampled_ms, 5), "timing": "ddt_tree_links + "
+                           "ddt_accept_sampled after the step (temperature 1, no top-k, vocab "
+                           f"{wl.vocab}, seeded N(0,1.5) logits); graph replay, L2 flushed, median"},
         "commit_kv": {"ms": round(commit_ms, 5), "timing": "ddt_commit_kv alone after the step, each "
                       "request committing its deepest root-to-leaf path; graph replay, L2 flushed, "
                       "median"},
@@ -343,6 +347,46 @@ def time_commit(st, stream, flush, reps=200):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
             st.commit_kv(stream=stream)
+    ts = []
+    for i in range(reps + 5):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            ts.append(a.elapsed_time(e))
+    st.check_device_errors()
+    return statistics.median(ts)
+
+
+def time_sampled(st, stream, flush, vocab, reps=200):
+    """Median time of the sampling accept (links + rejection sampling) on the
+    step's tree with seeded target logits, temperature 1 and no top-k."""
+    import torch
+    from tree_speculative_decoding_gb300 import ddt
+    dev = st.node_token.device
+    rows = st.node_token.numel()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    logits = torch.randn((rows, vocab), generator=gen, device=dev) * 1.5
+    coins = torch.rand((rows, st.wl.K + 1), generator=gen, device=dev)
+    temp = torch.ones(st.B, dtype=torch.float32, device=dev)
+    top_k = torch.zeros(st.B, dtype=torch.int32, device=dev)
+    fc, ns, ri = (torch.empty(rows, dtype=torch.int32, device=dev) for _ in range(3))
+    out = [torch.empty_like(t) for t in (st.accept_len, st.accepted_nodes, st.commit_tokens, st.bonus)]
+
+    def body(s):
+        ddt.ddt_tree_links(st.parent, st.qo_indptr, fc, ns, ri, stream=s)
+        ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, logits, temp, top_k, coins,
+                               st.wl.max_depth, *out, stream=s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        body(stream)
+        with torch.cuda.graph(g, stream=stream):
+            body(stream)
     ts = []
     for i in range(reps + 5):
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

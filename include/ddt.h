@@ -14,6 +14,8 @@
  *   ddt_verify_attn         tree-verify MLA attention in absorbed form
  *   ddt_accept              greedy walk: longest accepted chain + bonus token
  *   ddt_commit_kv           gather the accepted latents after the committed prefix
+ *   ddt_tree_links          the tree as first-child / next-sibling links
+ *   ddt_accept_sampled      tree rejection sampling with temperature and top-k
  *
  * Conventions for every entry point:
  *   - Pointers marked (device) must be device memory of the current CUDA
@@ -88,6 +90,7 @@ typedef enum {
 #define DDT_DEVERR_DEPTH        0x080u  /* accepted chain longer than max_depth + 1 */
 #define DDT_DEVERR_TIMEOUT      0x100u  /* a bounded wait inside a kernel ran out */
 #define DDT_DEVERR_ACCEPTED     0x200u  /* accept_len / accepted_nodes not an accepted path */
+#define DDT_DEVERR_SAMPLE       0x400u  /* sampling accept: links not a tree, or too few coins */
 
 const char *ddt_status_string(ddt_status s);
 int32_t ddt_abi_version(void);
@@ -278,6 +281,64 @@ ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
                       const int32_t *qo_indptr, const int32_t *target_argmax, int32_t batch,
                       int32_t max_depth, int32_t *accept_len, int32_t *accepted_nodes,
                       int32_t *commit_tokens, int32_t *bonus, void *stream);
+
+/*
+ * ddt_tree_links -- the tree in the format of a tree-sampling kernel.
+ * Page: "The DDTree CUDA Graph Fix ...", section "Temperature Support:
+ * Already Working for Linear, Planned for DDTree" (the parent lists become
+ * retrieve_index, retrieve_next_token and retrieve_next_sibling).
+ *
+ *   parent        (device) int32 [qo_indptr[batch]] from ddt_build_tree.
+ *   qo_indptr     (device) int32 [batch+1].
+ *   first_child   (device) int32 [qo_indptr[batch]] out: node n's lowest-index
+ *                 child (request-local index) or -1 (retrieve_next_token).
+ *   next_sibling  (device) int32 [qo_indptr[batch]] out: the next higher-index
+ *                 child of n's parent or -1 (retrieve_next_sibling).
+ *   retrieve_index(device) int32 [qo_indptr[batch]] out: qo_indptr[b] + n.
+ */
+ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32_t batch,
+                          int32_t *first_child, int32_t *next_sibling, int32_t *retrieve_index,
+                          void *stream);
+
+/*
+ * ddt_accept_sampled -- sampling accept: tree rejection sampling on the
+ * target distribution, the planned temperature support of "The DDTree CUDA
+ * Graph Fix ..." (section "Temperature Support: Already Working for Linear,
+ * Planned for DDTree").  The pages give no algorithm; the reading taken
+ * (target-only, deterministic drafts) is:
+ *   - p(n) = softmax(target_logits[n] / temperature[b]) over the tokens whose
+ *     logit is at least the top_k[b]-th largest (ties kept; all tokens when
+ *     top_k[b] <= 0 or >= vocab); temperature[b] <= 0 gives one-hot at the
+ *     argmax (lowest id on ties);
+ *   - at node n the children are tried in index order against the residual r
+ *     (p minus the tokens already rejected at n): child i, with token t, is
+ *     taken when coins[n][i] < r(t) / mass(r), otherwise t leaves r;
+ *   - if no child is taken, the bonus is the first token id whose cumulative
+ *     mass in r exceeds coins[n][coin_stride-1] * mass(r), and the walk stops.
+ * Every emitted token is then distributed as p.  At temperature 0 (or top_k
+ * 1) this is exactly ddt_accept with target_argmax = the logits' argmax.
+ * Probabilities are fp32 on the device, so a coin within ~1e-6 of a threshold
+ * may decide differently from an fp64 evaluation.
+ *
+ *   node_token, first_child, next_sibling, qo_indptr
+ *                 (device) the tree (ddt_build_tree) and its links (ddt_tree_links).
+ *   target_logits (device) float [qo_indptr[batch]][vocab]: target logits at each node.
+ *   temperature   (device) float [batch]; top_k (device) int32 [batch].
+ *   coins         (device) float [qo_indptr[batch]][coin_stride], uniform in [0,1):
+ *                 coin i for the i-th child tried at a node, the last for the
+ *                 bonus; coin_stride >= 1 + the largest number of children.
+ *   outputs       as for ddt_accept.
+ * Device checks: links that do not form the tree or a node with more
+ * children than coin_stride - 1 (DDT_DEVERR_SAMPLE; outputs unset), a walk
+ * deeper than max_depth (DDT_DEVERR_DEPTH).
+ */
+ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_child,
+                              const int32_t *next_sibling, const int32_t *qo_indptr,
+                              const float *target_logits, int32_t vocab, const float *temperature,
+                              const int32_t *top_k, const float *coins, int32_t coin_stride,
+                              int32_t batch, int32_t max_depth, int32_t *accept_len,
+                              int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus,
+                              void *stream);
 
 /*
  * ddt_commit_kv -- KV commit after acceptance (compaction of the accepted

@@ -98,6 +98,12 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.ddt_commit_kv(dummy, 0, dummy, dummy, dummy, dummy, dummy, 1, 7, None, None) == 1
     assert lib.ddt_commit_kv(dummy, 10, dummy, dummy, dummy, dummy, dummy, 1, 8, None, None) == 2
     assert lib.ddt_commit_kv(dummy, 10, dummy, dummy, dummy, dummy, dummy, 0, 7, None, None) == 0
+    assert lib.ddt_tree_links(None, dummy, 1, dummy, dummy, dummy, None) == 1
+    sa = [dummy] * 5
+    assert lib.ddt_accept_sampled(*sa, 0, dummy, dummy, dummy, 3, 1, 7, dummy, dummy, dummy, dummy,
+                                  None) == 1   # vocab 0
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 3, 1, 8, dummy, dummy, dummy,
+                                  dummy, None) == 2  # max_depth 8
     assert lib.ddt_verify_step(None, None) == 1
     assert lib.ddt_step_graph_create(None, None) == 1
     assert lib.ddt_step_graph_launch(None, None) == 1

@@ -384,3 +384,129 @@ def test_bad_budget_indptr_is_latched():
     status, bits = ddt.ddt_get_error()
     assert status == 5 and bits & 0x1
     assert ddt.ddt_get_error() == (0, 0)
+
+
+# ---------------------------------------------------------------- sampling accept
+
+def _links(st):
+    from tree_speculative_decoding_gb300 import ddt
+    T = st.node_token.numel()
+    fc, ns, ri = (torch.empty(T, dtype=torch.int32, device="cuda:0") for _ in range(3))
+    ddt.ddt_tree_links(st.parent, st.qo_indptr, fc, ns, ri)
+    return fc, ns, ri
+
+
+def _sampled(st, logits, temp, top_k, coins):
+    from tree_speculative_decoding_gb300 import ddt
+    fc, ns, _ = _links(st)
+    B, W = st.accepted_nodes.shape
+    out = [torch.empty(B, dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, W), dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, W), dtype=torch.int32, device="cuda:0"),
+           torch.empty(B, dtype=torch.int32, device="cuda:0")]
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
+    ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, dev(logits, np.float32),
+                           dev(temp, np.float32), dev(top_k, np.int32), dev(coins, np.float32),
+                           st.wl.max_depth, *out)
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    return [t.cpu().numpy() for t in out]
+
+
+@pytest.mark.parametrize("name", ["tiny_p21_b8_h8", "mixed_bs32_b16or32_h16", "edge"])
+def test_tree_links_match_oracle(name):
+    if name == "edge":
+        wl = workloads.make_workload("edge_links", 4246, 5, 4, [0, 64, 1, 300, 31],
+                                     [5, 0, 127, 31, 2], 16, 5000, 1.0)
+    else:
+        wl = workloads.preset(name)
+    st = _step(wl)
+    fc, ns, ri = _links(st)
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    ref = oracle.tree_links(st.parent.cpu().numpy(), wl.qo_indptr)
+    for g, r in zip((fc, ns, ri), ref):
+        np.testing.assert_array_equal(g.cpu().numpy(), r)
+
+
+def _sampling_case(wl, vocab, seed, chain_bias):
+    # target logits whose argmax sits on a child token at most nodes, so that
+    # walks go deep, plus uniform coins
+    st = _step(wl)
+    tok = st.node_token.cpu().numpy()
+    par = st.parent.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    logits = rng.normal(scale=1.5, size=(wl.total_q, vocab)).astype(np.float32)
+    for b in range(wl.B):
+        lo, hi = int(wl.qo_indptr[b]), int(wl.qo_indptr[b + 1])
+        for n in range(lo, hi):
+            kids = [c for c in range(n + 1, hi) if lo + par[c] == n]
+            if kids:
+                logits[n, tok[kids[0]] % vocab] += chain_bias
+    coins = rng.random((wl.total_q, wl.K + 1)).astype(np.float32)
+    return st, tok, par, logits, coins
+
+
+@pytest.mark.parametrize("name,vocab", [("tiny_p21_b8_h8", 512), ("mixed_bs32_b16or32_h16", 32768)])
+def test_sampled_accept_at_temperature_zero_is_greedy(name, vocab):
+    wl = workloads.preset(name)
+    st, tok, par, logits, coins = _sampling_case(wl, vocab, 5, 12.0)
+    got = _sampled(st, logits, np.zeros(wl.B), np.full(wl.B, 50), coins)
+    ref = oracle.accept(tok, par, wl.qo_indptr, logits.argmax(axis=1).astype(np.int32),
+                        wl.max_depth)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+    assert got[0].max() > 1
+
+
+@pytest.mark.parametrize("name,vocab,temp,top_k,bias", [
+    ("tiny_p21_b8_h8", 512, 0.8, 0, 10.0),
+    ("mixed_bs32_b16or32_h16", 32768, 1.0, 0, 11.5),
+    ("mixed_bs32_b16or32_h16", 32768, 0.7, 20, 7.0),
+])
+def test_sampled_accept_matches_oracle(name, vocab, temp, top_k, bias):
+    # probabilities are fp32 on the device and fp64 in the oracle: the seeds are
+    # chosen with no coin within fp32 rounding of a threshold, so the decisions
+    # (integers) must agree exactly
+    wl = workloads.preset(name)
+    st, tok, par, logits, coins = _sampling_case(wl, vocab, 11, bias)
+    t = np.full(wl.B, temp)
+    k = np.full(wl.B, top_k)
+    got = _sampled(st, logits, t, k, coins)
+    ref = oracle.accept_sampled(tok, par, wl.qo_indptr, logits, t, k, coins, wl.max_depth)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+    assert got[0].max() > 1
+
+
+def test_sampled_accept_emits_the_target_distribution():
+    # 4096 copies of one root with three leaf children (tokens 2, 5, 0) over a
+    # vocabulary of 8; the device's first emitted token must follow p(root)
+    from tree_speculative_decoding_gb300 import ddt
+    B, V, temp = 4096, 8, 0.9
+    rng = np.random.default_rng(3)
+    l = rng.normal(scale=1.2, size=V).astype(np.float32)
+    p = np.exp((l - l.max()) / temp)
+    p /= p.sum()
+    T = 4
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), B)
+    tok = np.tile(np.array([9, 2, 5, 0], np.int32), B)
+    qo = np.arange(B + 1, dtype=np.int32) * T
+    fc = np.tile(np.array([1, -1, -1, -1], np.int32), B)
+    ns = np.tile(np.array([-1, 2, 3, -1], np.int32), B)
+    logits = np.tile(l, (B * T, 1))
+    coins = rng.random((B * T, 4)).astype(np.float32)
+    d = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
+    out = [torch.empty(B, dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty(B, dtype=torch.int32, device="cuda:0")]
+    ddt.ddt_accept_sampled(d(tok, np.int32), d(fc, np.int32), d(ns, np.int32), d(qo, np.int32),
+                           d(logits, np.float32), d(np.full(B, temp), np.float32),
+                           d(np.zeros(B), np.int32), d(coins, np.float32), 2, *out)
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (0, 0)
+    first = out[2][:, 0].cpu().numpy()
+    freq = np.bincount(first, minlength=V) / B
+    assert np.abs(freq - p).max() < 4.5 * np.sqrt(0.25 / B)
+

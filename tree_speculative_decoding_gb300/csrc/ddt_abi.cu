@@ -264,6 +264,42 @@ ddt_status ddt_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
 }
 
+ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32_t batch,
+                          int32_t *first_child, int32_t *next_sibling, int32_t *retrieve_index,
+                          void *stream) {
+    if (!parent || !qo_indptr || !first_child || !next_sibling || !retrieve_index || batch < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_tree_links(parent, qo_indptr, batch, first_child, next_sibling,
+                                           retrieve_index, st->err, as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
+ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_child,
+                              const int32_t *next_sibling, const int32_t *qo_indptr,
+                              const float *target_logits, int32_t vocab, const float *temperature,
+                              const int32_t *top_k, const float *coins, int32_t coin_stride,
+                              int32_t batch, int32_t max_depth, int32_t *accept_len,
+                              int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus,
+                              void *stream) {
+    if (!node_token || !first_child || !next_sibling || !qo_indptr || !target_logits ||
+        !temperature || !top_k || !coins || !accept_len || !accepted_nodes || !commit_tokens ||
+        !bonus || batch < 0 || vocab < 1 || coin_stride < 1)
+        return DDT_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH) return DDT_ERR_UNSUPPORTED;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_accept_sampled(node_token, first_child, next_sibling, qo_indptr,
+                                               target_logits, vocab, temperature, top_k, coins,
+                                               coin_stride, batch, max_depth, accept_len,
+                                               accepted_nodes, commit_tokens, bonus, st->err,
+                                               as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 ddt_status ddt_get_error(void *stream, uint32_t *device_error) {
     DeviceState *st = device_state();
     if (!st) return DDT_ERR_CUDA;

@@ -736,6 +736,7 @@ cudaError_t attn_prepare_device() {
     if (e == cudaSuccess) e = attn_combine_prepare_device();
     if (e == cudaSuccess) e = tree_prepare_device();
     if (e == cudaSuccess) e = commit_prepare_device();
+    if (e == cudaSuccess) e = sample_prepare_device();
     if (e != cudaSuccess) return e;
     return attn_tc_prepare_device();
 }

@@ -75,6 +75,17 @@ cudaError_t launch_commit_kv(uint16_t *kv_pool, int64_t pool_rows, const int32_t
                              const int32_t *accept_len, const int32_t *accepted_nodes, int batch,
                              int max_depth, int32_t *new_len, unsigned int *err, cudaStream_t s);
 
+cudaError_t launch_tree_links(const int32_t *parent, const int32_t *qo_indptr, int batch,
+                              int32_t *first_child, int32_t *next_sibling, int32_t *retrieve_index,
+                              unsigned int *err, cudaStream_t s);
+cudaError_t launch_accept_sampled(const int32_t *node_token, const int32_t *first_child,
+                                  const int32_t *next_sibling, const int32_t *qo_indptr,
+                                  const float *logits, int vocab, const float *temperature,
+                                  const int32_t *top_k, const float *coins, int coin_stride, int batch,
+                                  int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
+                                  int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
+                                  cudaStream_t s);
+
 // Arguments of one verify-attention call as seen by the kernels.
 struct AttnArgs {
     const uint16_t *q;
@@ -112,6 +123,7 @@ cudaError_t attn_combine_prepare_device();
 // shared-memory carveout of the small stages' kernels (they overlap the attention)
 cudaError_t tree_prepare_device();
 cudaError_t commit_prepare_device();
+cudaError_t sample_prepare_device();
 
 // A kernel whose bounded mbarrier wait can never succeed: it latches
 // DDT_DEVERR_TIMEOUT and exits (the failure path, exercised without a fault).

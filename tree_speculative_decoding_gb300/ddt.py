@@ -49,6 +49,8 @@ def _load():
                                      P, P], i32),
         "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
         "ddt_commit_kv": ([P, i64, P, P, P, P, P, i32, i32, P, P], i32),
+        "ddt_tree_links": ([P, P, i32, P, P, P, P], i32),
+        "ddt_accept_sampled": ([P, P, P, P, P, i32, P, P, P, i32, i32, i32, P, P, P, P, P], i32),
         "ddt_get_error": ([P, P], i32),
         "ddt_selftest_wait_timeout": ([ctypes.c_uint32, P], i32),
         "ddt_verify_step": ([P, P], i32),
@@ -288,6 +290,38 @@ class StepGraph:
             self.close()
         except Exception:
             pass
+
+
+def ddt_tree_links(parent, qo_indptr, first_child, next_sibling, retrieve_index, stream=None):
+    """The tree as (first_child, next_sibling, retrieve_index) links."""
+    for n, t in (("parent", parent), ("qo_indptr", qo_indptr), ("first_child", first_child),
+                 ("next_sibling", next_sibling), ("retrieve_index", retrieve_index)):
+        _dev(t, torch.int32, n)
+    _check("ddt_tree_links", lib.ddt_tree_links(
+        _p(parent), _p(qo_indptr), qo_indptr.numel() - 1, _p(first_child), _p(next_sibling),
+        _p(retrieve_index), _stream(stream)))
+
+
+def ddt_accept_sampled(node_token, first_child, next_sibling, qo_indptr, target_logits,
+                       temperature, top_k, coins, max_depth, accept_len, accepted_nodes,
+                       commit_tokens, bonus, stream=None):
+    """Sampling accept: tree rejection sampling with temperature and top-k.
+    target_logits float32 [rows, vocab]; temperature float32 [B]; top_k int32 [B];
+    coins float32 [rows, coin_stride] uniform in [0, 1)."""
+    _dev(target_logits, torch.float32, "target_logits")
+    _dev(temperature, torch.float32, "temperature")
+    _dev(coins, torch.float32, "coins")
+    for n, t in (("node_token", node_token), ("first_child", first_child),
+                 ("next_sibling", next_sibling), ("qo_indptr", qo_indptr), ("top_k", top_k),
+                 ("accept_len", accept_len), ("accepted_nodes", accepted_nodes),
+                 ("commit_tokens", commit_tokens), ("bonus", bonus)):
+        _dev(t, torch.int32, n)
+    B = qo_indptr.numel() - 1
+    _check("ddt_accept_sampled", lib.ddt_accept_sampled(
+        _p(node_token), _p(first_child), _p(next_sibling), _p(qo_indptr), _p(target_logits),
+        target_logits.shape[1], _p(temperature), _p(top_k), _p(coins), coins.shape[1], B,
+        int(max_depth), _p(accept_len), _p(accepted_nodes), _p(commit_tokens), _p(bonus),
+        _stream(stream)))
 
 
 def ddt_get_error(stream=None):
