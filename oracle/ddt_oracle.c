@@ -510,12 +510,15 @@ int oracle_accept_sampled(const int32_t *node_token, const int32_t *parent,
                 }
                 for (int v = 0; v < vocab; ++v) p[v] /= z;
             }
-            /* the children, in index order, against the residual */
+            /* the children, in index order, against the residual; a node needs
+               one coin per child plus one for the bonus */
+            int nkids = 0;
+            for (int c = 1; c < T; ++c) nkids += parent[base + c] == cur;
+            if (nkids > coin_stride - 1) { status = OR_ERR_ARG; break; }
             double mass = 1.0;
             int next = -1, tried = 0;
             for (int c = 1; c < T; ++c) {
                 if (parent[base + c] != cur) continue;
-                if (tried >= coin_stride - 1) { status = OR_ERR_ARG; break; }
                 int t = node_token[base + c];
                 double pt = (t >= 0 && t < vocab) ? p[t] : 0.0;
                 if ((double)u[tried] < pt / mass) { next = c; break; }
