@@ -68,6 +68,7 @@ extern "C" {
 #define DDT_MAX_TOPK 16
 #define DDT_MAX_Q_LEN 128   /* budget + 1 */
 #define DDT_MAX_SPLITS 128
+#define DDT_MAX_VOCAB 262144 /* ddt_accept_sampled */
 
 typedef enum {
     DDT_OK = 0,
@@ -328,6 +329,7 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
  *                 coin i for the i-th child tried at a node, the last for the
  *                 bonus; coin_stride >= 1 + the largest number of children.
  *   outputs       as for ddt_accept.
+ * Supported: 1 <= vocab <= DDT_MAX_VOCAB.
  * Device checks: links that do not form the tree or a node with more
  * children than coin_stride - 1 (DDT_DEVERR_SAMPLE; outputs unset), a walk
  * deeper than max_depth (DDT_DEVERR_DEPTH).

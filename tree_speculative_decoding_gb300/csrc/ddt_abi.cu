@@ -288,7 +288,7 @@ ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_ch
         !temperature || !top_k || !coins || !accept_len || !accepted_nodes || !commit_tokens ||
         !bonus || batch < 0 || vocab < 1 || coin_stride < 1)
         return DDT_ERR_INVALID_ARG;
-    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH) return DDT_ERR_UNSUPPORTED;
+    if (max_depth < 1 || max_depth > DDT_MAX_DEPTH || vocab > DDT_MAX_VOCAB) return DDT_ERR_UNSUPPORTED;
     if (batch == 0) return DDT_OK;
     DeviceState *st = device_state();
     if (!st) return DDT_ERR_CUDA;

@@ -64,8 +64,36 @@ tree_links_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict_
 }
 
 // ------------------------------------------------------------- sampling accept
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxSteps = 64;  // 256-id steps per warp segment: vocabularies up to 16 * 64 * 256
+static_assert(kWarps * kMaxSteps * 256 == DDT_MAX_VOCAB, "vocabulary bound of the ABI");
+
+// Calls f(v, row[v]) for this thread's ids v = tid + k * kThreads with eight
+// loads in flight, so that one CTA streaming a vocabulary row is not bound by
+// one memory round trip per element.
+template <class F>
+__device__ __forceinline__ void for_each_logit(const float *row, int vocab, F f) {
+    for (int v0 = threadIdx.x; v0 < vocab; v0 += 8 * kThreads) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int v = v0 + k * kThreads;
+            x[k] = v < vocab ? row[v] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int v = v0 + k * kThreads;
+            if (v < vocab) f(v, x[k]);
+        }
+    }
+}
+
+// the row into L2 ahead of its passes (bulk prefetch: 16-byte aligned, whole 16-byte units)
+__device__ __forceinline__ void prefetch_row(const float *row, int vocab) {
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && (vocab & 3) == 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"(vocab * 4) : "memory");
+}
 
 __device__ __forceinline__ uint32_t order_key(float f) {  // larger float -> larger key
     const uint32_t u = __float_as_uint(f + 0.0f);  // -0 -> +0: equal floats, equal keys
@@ -73,10 +101,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {  // larger float -> lar
 }
 
 struct SampleSmem {
+    int tok[DDT_MAX_Q_LEN], fc[DDT_MAX_Q_LEN], ns[DDT_MAX_Q_LEN];  // the request's tree
+    int kid[DDT_MAX_TOPK + 1];       // children of the current node, in order
+    float kid_logit[DDT_MAX_TOPK + 1], kid_coin[DDT_MAX_TOPK + 1];
+    int nkid;
     float fred[kWarps];
     int ired[kWarps];
     unsigned hist[256];
-    float chunk[kThreads];
+    float step[kWarps][kMaxSteps];  // residual mass of each 256-id step of each warp's segment
     int removed[DDT_MAX_TOPK + 1];
     int nremoved;
     int decision;  // child taken, or -1
@@ -123,9 +155,25 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0;
         __syncthreads();
-        for (int v = threadIdx.x; v < vocab; v += kThreads) {
-            const unsigned key = order_key(row[v]);
-            if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
+        // equal bins within a warp are added once: after the first pass nearly all
+        // keys share their leading bits, and one shared-memory atomic per key would
+        // serialise on a handful of bins.  Eight loads in flight per thread.
+        const int lane = threadIdx.x & 31;
+        for (int v0 = threadIdx.x - lane; v0 < vocab; v0 += 8 * kThreads) {
+            unsigned key[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int v = v0 + k * kThreads + lane;
+                key[k] = v < vocab ? order_key(row[v]) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int v = v0 + k * kThreads + lane;
+                const bool in = v < vocab && (key[k] & mask) == prefix;
+                const unsigned bin = in ? (key[k] >> shift) & 255u : 256u;
+                const unsigned same = __match_any_sync(FULL, bin);
+                if (in && lane == __ffs(same) - 1) atomicAdd(&sm.hist[bin], (unsigned)__popc(same));
+            }
         }
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -166,59 +214,90 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
     const bool use_topk = !greedy && kk > 0 && kk < vocab;
     const float inv_t = greedy ? 0.f : 1.f / temp;
     const int width = max_depth + 1;
+    if (tid == 0 && T >= 1 && T <= DDT_MAX_Q_LEN) prefetch_row(logits + (size_t)base * vocab, vocab);
     pdl_wait();  // the tree and its links come from earlier kernels
     if (T < 1 || T > DDT_MAX_Q_LEN) {
         if (tid == 0) latch(err, DDT_DEVERR_QO_INDPTR);
         return;
     }
+    // the tree, once: every later walk step reads shared memory
+    for (int i = tid; i < T; i += kThreads) {
+        sm.tok[i] = node_token[base + i];
+        sm.fc[i] = first_child[base + i];
+        sm.ns[i] = next_sibling[base + i];
+    }
     int cur = 0, n = 1;
     if (tid == 0) path[0] = 0;
     int bon = -1;
     for (;;) {
+        __syncthreads();
         const float *row = logits + (size_t)(base + cur) * vocab;
         const float *u = coins + (size_t)(base + cur) * coin_stride;
-        // the argmax (and the max logit)
-        float lv = -INFINITY;
-        int li = vocab;
-        for (int v = tid; v < vocab; v += kThreads) {
-            const float x = row[v];
-            if (x > lv) { lv = x; li = v; }
+        // the children of cur, from the links; then their logits and coins, in parallel
+        if (tid == 0) {
+            int nk = 0;
+            for (int c = sm.fc[cur]; c >= 0; c = sm.ns[c]) {
+                if (c <= cur || c >= T || nk >= coin_stride - 1 || nk > DDT_MAX_TOPK) {
+                    nk = -1;  // links or coins do not fit the tree
+                    break;
+                }
+                sm.kid[nk++] = c;
+            }
+            sm.nkid = nk;
         }
+        __syncthreads();
+        const int nkid = sm.nkid;
+        if (nkid < 0) {
+            if (tid == 0) latch(err, DDT_DEVERR_SAMPLE);
+            return;
+        }
+        if (tid < nkid) {
+            const int t = sm.tok[sm.kid[tid]];
+            sm.kid_logit[tid] = (t >= 0 && t < vocab) ? row[t] : -INFINITY;
+            sm.kid_coin[tid] = u[tid];
+            prefetch_row(logits + (size_t)(base + sm.kid[tid]) * vocab, vocab);  // the next level's candidates
+        }
+        // the argmax, the max logit and (without top-k) the normaliser, in one
+        // online pass: sum e^{(x - m)/T} with m the running max of this thread
+        float lv = -INFINITY, ls = 0.f;
+        int li = vocab;
+        for_each_logit(row, vocab, [&](int v, float x) {
+            if (x > lv || (x == lv && v < li)) {
+                if (!greedy && x > lv) ls = (lv == -INFINITY ? 0.f : ls * __expf((lv - x) * inv_t));
+                lv = x;
+                li = v;
+            }
+            if (!greedy && !use_topk) ls += __expf((x - lv) * inv_t);
+        });
         float lmax;
         int amax;
         block_argmax(lv, li, sm, lmax, amax);
-        // kept set and normaliser
         unsigned thr = 0;
-        if (use_topk) thr = kth_largest_key(row, vocab, kk, sm);
         float z = 1.f;
-        if (!greedy) {
+        if (!greedy && !use_topk) {
+            z = block_sum(lv == -INFINITY ? 0.f : ls * __expf((lv - lmax) * inv_t), sm);
+        } else if (use_topk) {  // kept set first, then the normaliser over it
+            thr = kth_largest_key(row, vocab, kk, sm);
             float part = 0.f;
-            for (int v = tid; v < vocab; v += kThreads) {
-                const float x = row[v];
+            for_each_logit(row, vocab, [&](int, float x) {
                 if (order_key(x) >= thr) part += __expf((x - lmax) * inv_t);
-            }
+            });
             z = block_sum(part, sm);
         }
-        // p(v) of the target at this node (0 outside the kept set)
-        auto prob = [&](int v) -> float {
+        // p(v) of the target at this node (0 outside the kept set), from its logit
+        auto prob_of = [&](int v, float x) -> float {
             if (v < 0 || v >= vocab) return 0.f;
             if (greedy) return v == amax ? 1.f : 0.f;
-            const float x = row[v];
             return order_key(x) >= thr ? __expf((x - lmax) * inv_t) / z : 0.f;
         };
-        // the children against the residual (one thread: at most top-k children)
+        // the children against the residual (one thread, shared-memory values)
         if (tid == 0) {
             float mass = 1.f;
-            int taken = -1, i = 0, nrem = 0;
-            for (int c = first_child[base + cur]; c >= 0; c = next_sibling[base + c], ++i) {
-                if (c <= cur || c >= T || i >= coin_stride - 1 || i > DDT_MAX_TOPK) {
-                    latch(err, DDT_DEVERR_SAMPLE);  // links or coins do not fit the tree
-                    taken = -2;
-                    break;
-                }
-                const int t = node_token[base + c];
-                const float pt = prob(t);
-                if (u[i] < pt / mass) { taken = c; break; }
+            int taken = -1, nrem = 0;
+            for (int i = 0; i < nkid; ++i) {
+                const int t = sm.tok[sm.kid[i]];
+                const float pt = prob_of(t, sm.kid_logit[i]);
+                if (sm.kid_coin[i] < pt / mass) { taken = sm.kid[i]; break; }
                 mass -= pt;
                 sm.removed[nrem++] = t;
             }
@@ -228,7 +307,6 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         }
         __syncthreads();
         const int taken = sm.decision;
-        if (taken == -2) return;
         if (taken >= 0) {
             if (n >= width) {  // deeper than max_depth
                 if (tid == 0) latch(err, DDT_DEVERR_DEPTH);
@@ -237,7 +315,6 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
             if (tid == 0) path[n] = taken;
             ++n;
             cur = taken;
-            __syncthreads();
             continue;
         }
         // bonus: the first id whose cumulative residual mass exceeds coin * mass
@@ -247,54 +324,104 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         }
         const int nrem = sm.nremoved;
         const float target = u[coin_stride - 1] * sm.mass;
-        const int chunk = (vocab + kThreads - 1) / kThreads;
-        const int v0 = tid * chunk, v1 = min(vocab, v0 + chunk);
-        auto residual = [&](int v) -> float {
-            for (int r = 0; r < nrem; ++r)
-                if (sm.removed[r] == v) return 0.f;
-            return prob(v);
+        const int warp = tid >> 5, lane = tid & 31;
+        // warp w owns ids [w * seg, (w + 1) * seg) in steps of 256 ids, lane l
+        // holding ids [8l, 8l+8) of a step; each step's residual mass is kept
+        const int seg = ((vocab + kWarps - 1) / kWarps + 255) & ~255;
+        const int s0 = warp * seg, s1 = min(vocab, s0 + seg);
+        const int nsteps = s1 > s0 ? (s1 - s0 + 255) / 256 : 0;
+        auto residual_of = [&](int v, float x) -> float {
+            bool gone = false;
+            for (int r = 0; r < nrem; ++r) gone |= sm.removed[r] == v;
+            return gone ? 0.f : prob_of(v, x);
         };
-        float csum = 0.f;
-        int last_pos = -1;
-        for (int v = v0; v < v1; ++v) {
-            const float pv = residual(v);
-            csum += pv;
-            if (pv > 0.f) last_pos = v;
-        }
-        sm.chunk[tid] = csum;
-        __syncthreads();
-        if (tid == 0) {  // exclusive scan over the chunks, in id order
-            float acc = 0.f;
-            for (int t = 0; t < kThreads; ++t) {
-                const float s = sm.chunk[t];
-                sm.chunk[t] = acc;
-                acc += s;
+        // one step's lane-local running sums (loc), the lane total and its last id with mass
+        auto step_sums = [&](int st, float (&loc)[8], float &lsum, int &llast) {
+            const int b0 = s0 + 256 * st + 8 * lane;
+            float x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = b0 + k < s1 ? row[b0 + k] : 0.f;
+            lsum = 0.f;
+            llast = -1;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float pv = b0 + k < s1 ? residual_of(b0 + k, x[k]) : 0.f;
+                lsum += pv;
+                loc[k] = lsum;
+                if (pv > 0.f) llast = b0 + k;
             }
-            sm.bonus = -1;
+        };
+        int wlast = -1;
+        for (int st = 0; st < nsteps; ++st) {
+            float loc[8], lsum;
+            int llast;
+            step_sums(st, loc, lsum, llast);
+            for (int o = 16; o > 0; o >>= 1) {
+                lsum += __shfl_xor_sync(FULL, lsum, o);
+                llast = max(llast, __shfl_xor_sync(FULL, llast, o));
+            }
+            if (lane == 0) sm.step[warp][st] = lsum;
+            wlast = max(wlast, llast);
         }
+        if (lane == 0) sm.ired[warp] = wlast;
+        if (tid == 0) sm.bonus = -1;
         __syncthreads();
-        float cum = sm.chunk[tid];
-        if (cum <= target && cum + csum > target) {  // the one chunk where the prefix crosses
-            int pick = -1;
-            for (int v = v0; v < v1; ++v) {
-                const float pv = residual(v);
-                cum += pv;
-                if (cum > target) {
-                    pick = v;
-                    break;
+        // the crossing step: running prefixes over (warp, step) in id order, the same
+        // numbers in every thread, so at most one step qualifies
+        if (warp == 0) {
+            float pre = 0.f;
+            int cw = -1, cs = -1;
+            float cpre = 0.f;
+            for (int w = 0; w < kWarps && cw < 0; ++w) {
+                const int ws0 = w * seg, ws1 = min(vocab, ws0 + seg);
+                const int wn = ws1 > ws0 ? (ws1 - ws0 + 255) / 256 : 0;
+                for (int st = 0; st < wn; ++st) {
+                    const float nxt = pre + sm.step[w][st];
+                    if (pre <= target && target < nxt) {
+                        cw = w;
+                        cs = st;
+                        cpre = pre;
+                        break;
+                    }
+                    pre = nxt;
                 }
             }
-            sm.bonus = pick >= 0 ? pick : last_pos;  // rounding: the chunk's last id with mass
+            if (lane == 0) {  // scratch: the crossing warp, its step and the prefix before it
+                sm.decision = cw;
+                sm.mass = cpre;
+                sm.nkid = cs;
+            }
         }
-        // rounding fallback: the last id with residual mass
-        int lp = last_pos;
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
-        if ((tid & 31) == 0) sm.ired[tid >> 5] = lp;
         __syncthreads();
-        if (tid == 0) {
+        if (sm.decision == warp) {  // the crossing warp scans its one crossing step
+            float loc[8], lsum;
+            int llast;
+            step_sums(sm.nkid, loc, lsum, llast);
+            float incl = lsum;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float base_l = sm.mass + incl - lsum;  // this lane's prefix
+            const int b0 = s0 + 256 * sm.nkid + 8 * lane;
+            int mine = -1;  // the lane's first id with mass whose running sum passes the target
+            if (base_l + lsum > target)
+#pragma unroll
+                for (int k = 7; k >= 0; --k) {
+                    const bool mass_k = k == 0 ? loc[0] > 0.f : loc[k] > loc[k - 1];
+                    if (b0 + k < s1 && mass_k && base_l + loc[k] > target) mine = b0 + k;
+                }
+            const unsigned hit = __ballot_sync(FULL, mine >= 0);
+            int lastw = llast;
+            for (int o = 16; o > 0; o >>= 1) lastw = max(lastw, __shfl_xor_sync(FULL, lastw, o));
+            const int first = __shfl_sync(FULL, mine, hit ? __ffs(hit) - 1 : 0);
+            if (lane == 0) sm.bonus = hit ? first : lastw;  // rounding: the step's last id with mass
+        }
+        __syncthreads();
+        if (tid == 0 && sm.bonus < 0) {  // rounding put the target above the total
             int best = -1;
             for (int w = 0; w < kWarps; ++w) best = max(best, sm.ired[w]);
-            if (sm.bonus < 0) sm.bonus = best >= 0 ? best : amax;
+            sm.bonus = best >= 0 ? best : amax;
         }
         __syncthreads();
         bon = sm.bonus;
