@@ -58,7 +58,14 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                 print(r.stdout, r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if jobs or _stale(LIB, objs):
+    # objects of sources that no longer exist are dropped, and a changed set of
+    # objects relinks even when every remaining object is up to date
+    for old in glob.glob(os.path.join(BUILD, "*.o")):
+        if old not in objs:
+            os.remove(old)
+    manifest = os.path.join(BUILD, "objects.txt")
+    listed = open(manifest).read().split("\n") if os.path.exists(manifest) else None
+    if jobs or _stale(LIB, objs) or listed != objs:
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -66,6 +73,8 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
             print(r.stdout, r.stderr)
             raise RuntimeError("link of libddt.so failed")
         os.replace(tmp, LIB)
+        with open(manifest, "w") as f:
+            f.write("\n".join(objs))
     return LIB
 
 

@@ -732,8 +732,7 @@ cudaError_t attn_tc_prepare_device() {
 int attn_kv_tile() { return kNb; }
 
 cudaError_t attn_prepare_device() {
-    cudaError_t e = attn_simt_prepare_device();
-    if (e == cudaSuccess) e = attn_combine_prepare_device();
+    cudaError_t e = attn_combine_prepare_device();
     if (e == cudaSuccess) e = tree_prepare_device();
     if (e == cudaSuccess) e = commit_prepare_device();
     if (e == cudaSuccess) e = sample_prepare_device();

@@ -116,8 +116,6 @@ cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s);
 int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms);
 cudaError_t attn_tc_prepare_device();
 // CUDA-core kernel of the same pass (same arguments and outputs)
-cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
-cudaError_t attn_simt_prepare_device();
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
 cudaError_t attn_combine_prepare_device();
 // shared-memory carveout of the small stages' kernels (they overlap the attention)
