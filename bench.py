@@ -1,8 +1,8 @@
 """Benchmark of one DDTree verify step on GB300.
 
-A step is the whole hot path on one batch: ddt_build_tree ->
-ddt_compile_visibility -> ddt_verify_attn (split-KV partial + combine) ->
-ddt_accept, captured once in a CUDA graph and replayed.  Inputs are seeded
+A step is the whole hot path on one batch: ddt_build_tree_visibility (tree
+build and mask compile, one launch) -> ddt_verify_attn (split-KV partial +
+combine) -> ddt_accept, captured once in a CUDA graph and replayed.  Inputs are seeded
 and synthetic (workload "single_p4096_b32_h64": 1 request, prefix 4096,
 budget 32, 64 heads, 576-wide bf16 latent rows in a 65536-row pool) and
 resident in HBM; L2 is flushed (a 256 MiB write) before every timed step.
@@ -11,7 +11,9 @@ The reported metric is verify-attention TFLOP/s: algorithmic attention FLOPs
 (2 * (576 + 512) per visible (query-head, kv) pair) per second of the whole
 step.  KV GB/s, steps/s, a roofline object for ddt_verify_attn (timed with
 CUDA events inside the same region), an end-to-end figure through host
-buffers, and the CPU oracle timed on the host cores are printed beside it.
+buffers (one packed copy each way), the CPU oracle timed on the host cores,
+and the times of the KV commit and the sampling accept on their own (not part
+of the step) are printed beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -430,7 +432,7 @@ def cpu_baseline(wl, seconds=10.0):
     dt = time.perf_counter() - t0
     return {"value": round(total / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{reps} full oracle verify steps of {WORKLOAD} (tree, mask, fp64 attention "
+            "sample": f"{reps} full oracle verify steps of {wl.name} (tree, mask, fp64 attention "
                       f"over all {wl.total_q * wl.H} rows, accept) in {dt:.1f} s"}
 
 
