@@ -218,6 +218,38 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         return;
     }
 
+    // ---- loads that need no set-up, issued before it so that the barrier
+    // init, the tensor-memory allocation and the cluster sync run under their
+    // latency: the softmax warps' Q row, the producers' first kStages blocks of
+    // kv slots ----
+    const int mma_warp = rank ? 4 : 6;
+    const bool producer = warp >= 4 && warp != mma_warp;
+    const int half = (warp == (rank ? 5 : 4)) ? 0 : 1;  // producers: kv rows [32 half, 32 half + 32)
+    // slot of this producer lane's kv row of block j
+    auto fetch_slot = [&](int j) {
+        return a.kv_indices[kv0 + min(c_begin + j * kNb + 32 * half + lane, c_end - 1)];  // rows past the end reuse a valid one
+    };
+    int slot_ahead[kStages];
+    if (producer) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) slot_ahead[s] = (s < nblk) ? fetch_slot(s) : 0;
+    }
+    const int r = tid;  // row within the tile for warps 0-3
+    uint4 xl[32], xr[4];
+    if (warp < 4) {
+        const bool valid = r < rows_valid;
+        const int rr = row0 + r;
+        const uint4 *src = nullptr;
+        if (valid) {
+            const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
+            src = reinterpret_cast<const uint4 *>(a.q + grow * DDT_D);
+        }
+#pragma unroll
+        for (int v = 0; v < 32; ++v) xl[v] = valid ? src[(256 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) xr[v] = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
+    }
+
     // ---- setup ----
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) {
@@ -239,8 +271,6 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     const uint32_t tmem = *holder;
     cluster_sync();  // both CTAs' barriers exist before any remote access
 
-    // softmax warps: this CTA's half of Q into tensor memory (thread = row = lane)
-    const int r = tid;  // row within the tile for warps 0-3
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     // Every MMA accumulates (enable-input-D set): an MMA that overwrites its
     // accumulator right behind a tcgen05.commit waits for the committed MMAs to
@@ -253,21 +283,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         for (int q = 0; q < kNb / 32; ++q) tmem_st32(tmem + lane_off + kColS + kNb * sb + 32 * q, z);
         tmem_wait_st();
     };
-    if (warp < 4) {
+    if (warp < 4) {  // this CTA's half of Q into tensor memory (thread = row = lane)
         uint32_t w[32];
-        const bool valid = r < rows_valid;
-        const int rr = row0 + r;
-        const uint4 *src = nullptr;
-        if (valid) {
-            const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
-            src = reinterpret_cast<const uint4 *>(a.q + grow * DDT_D);
-        }
-        // all of the row's loads first (one memory round trip), then the stores
-        uint4 xl[32], xr[4];
-#pragma unroll
-        for (int v = 0; v < 32; ++v) xl[v] = valid ? src[(256 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) xr[v] = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int part = 0; part < 4; ++part) {  // latent: 4 x 64 dims
 #pragma unroll
@@ -293,14 +310,13 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     // Warp w issues on sub-partition w % 4.  The MMA warp spins on barriers, so
     // it goes next to a non-owner softmax warp: warp 6 (with warp 2) in rank 0,
     // where warps 0-1 own rows, and warp 4 (with warp 0) in rank 1.
-    const int mma_warp = rank ? 4 : 6;
     if (warp < 4 || warp == mma_warp) {
         tc_fence_before();
         named_barrier(1, 160);
         tc_fence_after();
     }
 
-    if (warp >= 4 && warp != mma_warp) {
+    if (producer) {
         // ================= producers: gather this CTA's five boxes per kv row =================
         // Warp 4 moves kv rows [0, 32) of each block, warp 6 rows [32, 64).  One
         // warp instruction moves one 128-byte box line of four kv rows: lane =
@@ -308,19 +324,11 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         // the 128-byte swizzle (chunk ^ (row & 7)) that the MMA descriptors
         // expect.  Each lane arrives on the stage barrier once its own copies
         // have landed (64 arrivals per stage).
-        const int half = (warp == (rank ? 5 : 4)) ? 0 : 1;
         const int sub = lane >> 3, chunk = lane & 7;
         const char *pool = reinterpret_cast<const char *>(a.kv_pool);
-        // slot of this warp's kv row `lane` of block j.  Each is loaded one
-        // stage ring ahead (slot_ahead[s] holds block j's while stage s gathers
-        // block j - kStages), so the first kStages blocks need one index round
-        // trip between them and later index loads overlap the stage waits.
-        auto fetch_slot = [&](int j) {
-            return a.kv_indices[kv0 + min(c_begin + j * kNb + 32 * half + lane, c_end - 1)];  // rows past the end reuse a valid one
-        };
-        int slot_ahead[kStages];
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) slot_ahead[s] = (s < nblk) ? fetch_slot(s) : 0;
+        // slot_ahead[s] holds block j's slot while stage s gathers block
+        // j - kStages: each slot is loaded one stage ring ahead (the first
+        // kStages before the set-up), so index loads overlap the stage waits.
         bool run = true;
         for (int j0 = 0; run && j0 < nblk; j0 += kStages) {
 #pragma unroll
