@@ -294,6 +294,16 @@ def test_step_graph_reports_a_host_check_and_makes_no_graph():
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("B", [256, 300])
+def test_large_batches_cover_both_dispatch_orders(B):
+    # up to 256 requests the kernel starts the longest first; beyond, block order
+    rng = np.random.default_rng(B)
+    prefix = rng.integers(0, 90, B)
+    budget = rng.integers(0, 6, B)
+    wl = workloads.make_workload(f"batch{B}", 7000 + B, B, 4, prefix, budget, 4, 300, 1.5)
+    _full_check(wl, n_rows=600)
+
+
 def test_chain_tree_equals_causal_prefill():
     wl = workloads.make_workload("chain", 77, 1, 4, [40], [7], 1, 300, 2.0)
     st, (tok, par, dep) = _full_check(wl, n_rows=10 ** 9)
