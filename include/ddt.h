@@ -238,10 +238,13 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
  * that loads the library holds until the process exits.
  *
  * Arguments, outputs and errors are those of ddt_verify_attn minus the
- * workspace.  If the chosen (or requested) split count needs more scratch
- * than DDT_NOALLOC_SCRATCH_BYTES (see ddt_verify_attn_workspace_size), the
- * call returns DDT_ERR_WORKSPACE and launches nothing; pass a smaller
- * num_splits (1 needs no scratch) or use ddt_verify_attn.
+ * workspace.  With num_splits = 0 the library picks the split count as
+ * ddt_verify_attn does, but only among the counts whose split results fit
+ * DDT_NOALLOC_SCRATCH_BYTES (see ddt_verify_attn_workspace_size), down to 1,
+ * which needs no scratch; so a long kv range over many rows may run with
+ * fewer splits here than through ddt_verify_attn.  An explicit num_splits
+ * that needs more scratch than that returns DDT_ERR_WORKSPACE and launches
+ * nothing.
  * The first call on a device looks up the array's device address for that
  * device; make that first call before any stream capture.  All calls share
  * the one array: calls that overlap on the GPU (other streams, other

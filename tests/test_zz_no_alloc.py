@@ -70,3 +70,31 @@ def test_noalloc_rejects_scratch_beyond_its_capacity(step):
                                     max_kv_len=step.max_kv_len, num_splits=16)
     assert e.value.status == 3            # DDT_ERR_WORKSPACE, nothing launched
     assert bool((out == 0).all())
+
+
+def test_noalloc_own_split_choice_fits_its_scratch():
+    # one request, prefix 32768, budget 64, 64 heads: the split count the
+    # workspace entry point picks needs more than the fixed scratch, so the
+    # allocation-free call must pick a smaller one rather than refuse
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tree_speculative_decoding_gb300 import ddt
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("noalloc_long", 0xA110D, 1, 64, [32768], [64], 8, 32768, 3.0)
+    st = VerifyStep(wl, "cuda:0")
+    st.run()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    assert ddt.ddt_verify_attn_workspace_size(st.total_q, st.H, st.num_splits) > \
+        ddt.NOALLOC_SCRATCH_BYTES
+    out = torch.full_like(st.out, float("nan"))
+    lse = torch.full_like(st.lse, float("nan"))
+    ddt.ddt_verify_attn_noalloc(st.q, st.kv_pool, st.kv_indices, st.kv_indptr, st.qo_indptr,
+                                st.mask, st.mask_indptr, st.wl.scale, out, lse,
+                                max_q_len=st.max_q_len, max_kv_len=st.max_kv_len, num_splits=0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    _close(out, st.out)
+    _close(lse, st.lse)
+    status, bits = ddt.ddt_get_error()
+    assert status == 0, hex(bits)

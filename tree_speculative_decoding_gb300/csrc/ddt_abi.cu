@@ -401,5 +401,9 @@ unsigned int *device_error_word() {
     DeviceState *st = device_state();
     return st ? st->err : nullptr;
 }
+int device_sm_count() {
+    DeviceState *st = device_state();
+    return st ? st->num_sms : 148;
+}
 }  // namespace ddt
 

@@ -759,13 +759,15 @@ cudaError_t attn_prepare_device() {
 // with at least 4 blocks per split.  For one request this picks the best count
 // measured (4 at prefix 4096, 9 at prefix 131072, where 297 clusters fill four
 // waves almost exactly).
-int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms) {
+int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms,
+                       int max_splits) {
     const long long tiles = (long long)batch * (((long long)max_q_len * num_heads + kRows - 1) / kRows);
     const long long pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
     if (batch > 1 && tiles >= pairs) return 1;
     const long long blocks = ((long long)max_kv_len + kNb - 1) / kNb;
     long long smax = blocks / 4;  // keep >= 4 blocks per split
     if (smax > DDT_MAX_SPLITS) smax = DDT_MAX_SPLITS;
+    if (smax > max_splits) smax = max_splits;
     if (smax < 1) smax = 1;
     constexpr long long kFixedBlocks = 8;
     long long best = 1, best_cost = -1;

@@ -113,7 +113,9 @@ struct AttnArgs {
 
 // Split-KV partial pass (tensor-core kernel) and its sizing rules.
 cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s);
-int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms);
+// the split count for these bounds, at most max_splits (>= 1)
+int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, int num_sms,
+                       int max_splits = DDT_MAX_SPLITS);
 cudaError_t attn_tc_prepare_device();
 // CUDA-core kernel of the same pass (same arguments and outputs)
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
@@ -136,5 +138,7 @@ cudaError_t attn_prepare_device();
 
 // Device address of the current device's error word (null on failure).
 unsigned int *device_error_word();
+// the current device's SM count (after the same one-time set-up)
+int device_sm_count();
 
 }  // namespace ddt

@@ -70,9 +70,15 @@ extern "C" ddt_status ddt_verify_attn_noalloc(
     void *scratch = scratch_address();
     if (!err || !scratch) return DDT_ERR_CUDA;
 
-    int splits = num_splits > 0
-        ? num_splits
-        : ddt_verify_attn_num_splits(batch, num_heads, max_q_len, max_kv_len, 0);
+    int splits = num_splits;
+    if (splits == 0) {  // the library's choice, among the counts whose partials fit the scratch
+        int cap = DDT_MAX_SPLITS;
+        while (cap > 1 && ddt_verify_attn_workspace_size(total_q, num_heads, cap) >
+                              (size_t)DDT_NOALLOC_SCRATCH_BYTES)
+            --cap;
+        splits = ddt::attn_choose_splits(batch, num_heads, max_q_len, max_kv_len,
+                                         ddt::device_sm_count(), cap);
+    }
     const int tile = ddt::attn_kv_tile();
     int split_cols = (max_kv_len + splits - 1) / splits;
     split_cols = (split_cols + tile - 1) / tile * tile;

@@ -215,8 +215,9 @@ def ddt_verify_attn_noalloc(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, 
     device-synchronising cudaMalloc is not allowed): the split scratch is a
     fixed 32 MiB array inside libddt.so, so neither this wrapper nor the call
     allocates on the device.  Calls overlapping on the GPU race on that
-    array.  Raises DDTError(DDT_ERR_WORKSPACE) when the split count needs more
-    scratch than the array holds."""
+    array.  num_splits = 0 takes the library's choice among the counts that
+    fit the array; an explicit count that needs more scratch than the array
+    holds raises DDTError(DDT_ERR_WORKSPACE)."""
     _dev(q, torch.bfloat16, "q")
     _dev(kv_pool, torch.bfloat16, "kv_pool")
     _dev(out, torch.float32, "out")
