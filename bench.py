@@ -267,6 +267,7 @@ def run_device(args, rank, world, local_rank):
 
     commit_ms = time_commit(st, stream, flush)
     sampled_ms = time_sampled(st, stream, flush, wl.vocab)
+    degenerate = time_degenerate(dev, stream, flush)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     ms_per_step = elapsed_max * 1e3 / args.steps
     value = flops_all / elapsed_max / 1e12
@@ -314,6 +315,9 @@ def run_device(args, rank, world, local_rank):
         "commit_kv": {"ms": round(commit_ms, 5), "timing": "ddt_commit_kv alone after the step, each "
                       "request committing its deepest root-to-leaf path; graph replay, L2 flushed, "
                       "median"},
+        "degenerate": dict(degenerate, timing="each graph replayed on its own after the step, "
+                           "L2 flushed, median; autoregressive = the whole step at budget 0, "
+                           "prefill = causal mask compile + attention for 128 new tokens"),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -321,6 +325,28 @@ def run_device(args, rank, world, local_rank):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def replay_median(body, stream, flush, reps):
+    """Median device time of `body(stream)` captured as one CUDA graph and
+    replayed `reps` times after 5 untimed replays, L2 flushed before each."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            body(stream)
+    ts = []
+    for i in range(reps + 5):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            e.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            ts.append(a.elapsed_time(e))
+    return statistics.median(ts)
 
 
 def time_commit(st, stream, flush, reps=200):
@@ -345,23 +371,9 @@ def time_commit(st, stream, flush, reps=200):
         acc[b, :len(path)] = path
     st.accept_len.copy_(torch.from_numpy(alen))
     st.accepted_nodes.copy_(torch.from_numpy(acc))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g, stream=stream):
-            st.commit_kv(stream=stream)
-    ts = []
-    for i in range(reps + 5):
-        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            flush.zero_()
-            a.record(stream)
-            g.replay()
-            e.record(stream)
-        torch.cuda.synchronize()
-        if i >= 5:
-            ts.append(a.elapsed_time(e))
+    ms = replay_median(lambda s: st.commit_kv(stream=s), stream, flush, reps)
     st.check_device_errors()
-    return statistics.median(ts)
+    return ms
 
 
 def time_sampled(st, stream, flush, vocab, reps=200):
@@ -384,24 +396,46 @@ def time_sampled(st, stream, flush, vocab, reps=200):
         ddt.ddt_tree_links(st.parent, st.qo_indptr, fc, ns, ri, stream=s)
         ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, logits, temp, top_k, coins,
                                st.wl.max_depth, *out, stream=s)
-    g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         body(stream)
-        with torch.cuda.graph(g, stream=stream):
-            body(stream)
-    ts = []
-    for i in range(reps + 5):
-        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            flush.zero_()
-            a.record(stream)
-            g.replay()
-            e.record(stream)
-        torch.cuda.synchronize()
-        if i >= 5:
-            ts.append(a.elapsed_time(e))
+    ms = replay_median(body, stream, flush, reps)
     st.check_device_errors()
-    return statistics.median(ts)
+    return ms
+
+
+def time_degenerate(dev, stream, flush, reps=200):
+    """The path's degenerate shapes, one request after a prefix of 4096 at 64
+    heads: the autoregressive step (budget 0; tree, mask, attention and
+    accept) and a prefill chunk of 128 new tokens under a causal mask (the
+    tree replaced by a chain; mask compile and attention)."""
+    import torch
+    from tree_speculative_decoding_gb300 import workloads
+    from tree_speculative_decoding_gb300.metrics import attn_flops, kv_bytes
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    res = {}
+    for name in ("ar_p4096_b0_h64", "prefill_p4096_t128_h64"):
+        wl = workloads.preset(name)
+        st = VerifyStep(wl, dev)
+        if name.startswith("prefill"):
+            st.set_causal_chain()
+
+            def body(s, st=st):
+                st.compile_visibility(stream=s)
+                st.verify_attn(stream=s)
+        else:
+            def body(s, st=st):
+                st.run(stream=s)
+        with torch.cuda.stream(stream):
+            body(stream)
+        torch.cuda.synchronize()
+        st.check_device_errors()
+        flops = attn_flops(wl.prefix_len, st.depth.cpu().numpy(), wl.qo_indptr, wl.H)
+        ms = replay_median(body, stream, flush, reps)
+        st.check_device_errors()
+        res[name] = {"ms": round(ms, 5), "tflops": round(flops / ms / 1e9, 3),
+                     "kv_gbs": round(kv_bytes(wl.kv_indptr) / ms / 1e6, 2),
+                     "q_len": int(wl.q_len[0]), "num_splits": st.num_splits}
+    return res
 
 
 def oracle_step(wl, rows=None):

@@ -310,6 +310,58 @@ def test_chain_tree_equals_causal_prefill():
     assert dep.tolist() == list(range(8))
 
 
+def _causal_chunk(wl):
+    """The step's tree replaced by a causal chain, then the mask and the
+    attention: a prefill chunk of q_len tokens after each prefix."""
+    st = _step(wl)
+    st.set_causal_chain()
+    st.compile_visibility()
+    st.verify_attn()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    par = st.parent.cpu().numpy()
+    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    got = st.mask.cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(got, mask)
+    # the chain's mask is the causal one: row i of request b sees columns [0, P_b + i]
+    for b in range(wl.B):
+        P, T = int(wl.prefix_len[b]), int(wl.q_len[b])
+        W = (P + T + 31) // 32
+        words = np.ascontiguousarray(got[mip[b]:mip[b + 1]]).astype("<u4")
+        bits = np.unpackbits(words.view(np.uint8), bitorder="little").reshape(T, W * 32)
+        causal = np.arange(W * 32)[None, :] <= (P + np.arange(T))[:, None]
+        np.testing.assert_array_equal(bits.astype(bool), causal)
+    return st, mask, mip
+
+
+@pytest.mark.parametrize("H", [1, 16])
+def test_prefill_chunk_of_128_tokens_is_causal_attention(H):
+    # q_len 128 after prefixes 300, 0 and 33 (a ragged word boundary), every row
+    wl = workloads.make_workload(f"prefill{H}", 4250 + H, 3, H, [300, 0, 33], [127, 127, 60], 8,
+                                 5000, 1.0)
+    st, mask, mip = _causal_chunk(wl)
+    _check_attn(st, wl, mask, mip, _sample_rows(wl, 10 ** 9))
+
+
+def test_prefill_chunk_full_size():
+    # the timed shape: 128 new tokens after a prefix of 4096, 64 heads, sampled rows
+    wl = workloads.preset("prefill_p4096_t128_h64")
+    st, mask, mip = _causal_chunk(wl)
+    _check_attn(st, wl, mask, mip, _sample_rows(wl, 384))
+
+
+def test_autoregressive_steps_budget_zero():
+    # budget 0 everywhere: q_len 1, the plain decode step; the timed single
+    # request at 64 heads, then a ragged batch of 64 at 8 heads
+    st, (tok, par, dep) = _full_check(workloads.preset("ar_p4096_b0_h64"), n_rows=10 ** 9)
+    assert st.accept_len.item() == 1 and par.tolist() == [-1]
+    rng = np.random.default_rng(5)
+    wl = workloads.make_workload("ar64", 4260, 64, 8, rng.integers(0, 3000, 64), np.zeros(64, int),
+                                 4, 1000, 1.0)
+    st, _ = _full_check(wl, n_rows=10 ** 9)
+    assert (st.accept_len.cpu().numpy() == 1).all()
+
+
 def test_cuda_graph_capture_and_replay():
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
     wl = workloads.make_workload("graph", 31, 3, 16, [500, 20, 1100], [16, 9, 32], 8, 3000, 2.0)

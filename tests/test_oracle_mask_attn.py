@@ -139,6 +139,21 @@ def test_chain_equals_causal_prefill(oracle_mod):
     np.testing.assert_allclose(out.reshape(c["T"], c["H"], 512), ref, rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("prefix", [[0], [31, 33], [4096]])
+def test_chain_of_128_gives_the_causal_mask(oracle_mod, prefix):
+    # parent[i] = i - 1 over q_len 128 (the largest): row i sees columns [0, P + i]
+    B, T = len(prefix), 128
+    par = np.tile(np.arange(-1, T - 1, dtype=np.int32), B)
+    qo = (np.arange(B + 1) * T).astype(np.int32)
+    mask, mip = oracle_mod.compile_visibility(par, qo, np.array(prefix, np.int32))
+    for b, P in enumerate(prefix):
+        W = (P + T + 31) // 32
+        words = np.ascontiguousarray(mask[mip[b]:mip[b + 1]]).astype("<u4")
+        bits = np.unpackbits(words.view(np.uint8), bitorder="little").reshape(T, W * 32)
+        causal = np.arange(W * 32)[None, :] <= (P + np.arange(T))[:, None]
+        np.testing.assert_array_equal(bits.astype(bool), causal)
+
+
 def test_single_visible_column_returns_its_value_row(oracle_mod):
     c = _tiny_case(oracle_mod, 5, 0, 2, 2, 3, H=4)     # prefix 0: the root sees only itself
     out, lse = oracle_mod.verify_attn(c["q"], c["pool"], c["slots"], c["kvp"], c["qo"], c["mask"],

@@ -108,6 +108,24 @@ class VerifyStep:
         ddt.ddt_compile_visibility(self.parent, self.qo_indptr, self.prefix_len, self.mask_indptr,
                                    self.mask, stream)
 
+    def set_causal_chain(self):
+        """Replaces the tree by a chain, parent[i] = i - 1 (depth i) within each
+        request.  Engine page, "The Core Design Problem: A Unified Forward Pass":
+        prefill, decode and tree verify are one forward that differs only in
+        its mask.  The mask compiled from it is causal over the request's q_len
+        new tokens, so compile_visibility followed by verify_attn is a prefill
+        chunk after the prefix; budget 0 (q_len 1) is the autoregressive step.
+        A blocking host-to-device copy: call it outside stream capture."""
+        par = np.empty(self.total_q, np.int32)
+        dep = np.empty(self.total_q, np.int32)
+        qo = self.wl.qo_indptr
+        for b in range(self.B):
+            lo, hi = int(qo[b]), int(qo[b + 1])
+            par[lo:hi] = np.arange(-1, hi - lo - 1, dtype=np.int32)
+            dep[lo:hi] = np.arange(hi - lo, dtype=np.int32)
+        self.parent.copy_(torch.from_numpy(par))
+        self.depth.copy_(torch.from_numpy(dep))
+
     def build_tree_visibility(self, stream=None):
         ddt.ddt_build_tree_visibility(self.topk_logp, self.topk_ids, self.root_id, self.budget,
                                       self.qo_indptr, self.prefix_len, self.mask_indptr,

@@ -241,12 +241,25 @@ PRESETS = {
 }
 
 
+# The degenerate shapes of the same path, one request after a prefix of 4096
+# at 64 heads: the autoregressive step (budget 0, q_len 1) and a prefill chunk
+# of 128 new tokens (budget 127, whose tree the caller replaces by a causal
+# chain).  Seeds continue the series above.
+DEGENERATE = {
+    "ar_p4096_b0_h64": dict(k=6, B=1, H=64, prefix=("fixed", 4096), budget=("fixed", 0), K=8,
+                            vocab=32768, sigma=3.0, pool_rows=65536),
+    "prefill_p4096_t128_h64": dict(k=7, B=1, H=64, prefix=("fixed", 4096),
+                                   budget=("fixed", 127), K=8, vocab=32768, sigma=3.0,
+                                   pool_rows=65536),
+}
+
+
 def preset_seed(name: str) -> int:
-    return 0xDD7E0000 + PRESETS[name]["k"]
+    return 0xDD7E0000 + {**PRESETS, **DEGENERATE}[name]["k"]
 
 
 def preset(name: str, fill_pool: bool = True) -> Workload:
-    p = PRESETS[name]
+    p = {**PRESETS, **DEGENERATE}[name]
     seed = preset_seed(name)
     B = p["B"]
     kind = p["prefix"][0]
