@@ -12,10 +12,12 @@ The reported metric is verify-attention TFLOP/s: algorithmic attention FLOPs
 step.  KV GB/s, steps/s, a roofline object for ddt_verify_attn (timed with
 CUDA events inside the same region), an end-to-end figure through host
 buffers (one packed copy each way), the CPU oracle timed on the host cores,
-and the times of the KV commit and the sampling accept on their own (not part
-of the step) are printed beside it.
+the times of the KV commit and the sampling accept on their own (not part of
+the step), and of the autoregressive step and a 128-token prefill chunk of the
+same path, are printed beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --timeline [--workload W]   # per-kernel offsets inside a step
 
 For N > 1 (torchrun) every rank runs its own copy of the workload (weak
 scaling, no collective on the data path); the time is the max over ranks.
@@ -438,6 +440,66 @@ def time_degenerate(dev, stream, flush, reps=200):
     return res
 
 
+def step_timeline(workload, reps=50):
+    """Where the time goes inside one step: the step graph replayed `reps`
+    times (L2 flushed before each) under the CUDA activity trace of
+    torch.profiler; per kernel, the median start and end in µs from the first
+    kernel of the step.  Diagnostic only: no reported figure comes from a
+    traced run."""
+    import re
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    from tree_speculative_decoding_gb300 import workloads
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.preset(workload)
+    st = VerifyStep(wl, "cuda:0")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        st.run(stream=stream)
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            st.run(stream=stream)
+
+    def replays(n):
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                g.replay()
+        torch.cuda.synchronize()
+    replays(10)
+    with profile(activities=[ProfilerActivity.CUDA]):   # the tracer's own start-up
+        replays(3)
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        replays(reps)
+    kernels = sorted((e.time_range.start, e.time_range.end, e.name) for e in prof.events()
+                     if e.device_type.name == "CUDA")
+    steps, cur = [], None
+    for t0, t1, name in kernels:
+        if "FillFunctor" in name:      # the L2 flush opens each step
+            cur = []
+            steps.append(cur)
+        elif cur is not None:
+            m = re.search(r"(\w+_kernel)", name)
+            cur.append((t0, t1, m.group(1) if m else name[:48]))
+    rows = {}
+    for k in steps[5:]:
+        if not k:
+            continue
+        base = k[0][0]
+        for t0, t1, name in k:
+            rows.setdefault(name, []).append((t0 - base, t1 - base))
+    st.check_device_errors()
+    out = {name: {"start_us": round(statistics.median(a for a, _ in v), 2),
+                  "end_us": round(statistics.median(b for _, b in v), 2), "steps": len(v)}
+           for name, v in rows.items()}
+    return {"workload": workload, "num_splits": st.num_splits, "kernels": out}
+
+
 def oracle_step(wl, rows=None):
     """One verify step of the CPU oracle; returns attention FLOPs of the rows it computed."""
     import oracle
@@ -511,11 +573,16 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="print per-kernel start/end offsets inside one step (diagnostic)")
     ap.add_argument("--source-digests", action="store_true",
                     help="print the digests of the profiled attention sources and exit")
     args = ap.parse_args(argv)
     if args.source_digests:
         print(json.dumps({rel: source_digest(rel) for rel in PROFILE_TRAFFIC["sources"]}, indent=1))
+        return
+    if args.timeline:
+        print(json.dumps(step_timeline(args.workload)), flush=True)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
