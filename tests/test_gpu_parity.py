@@ -525,6 +525,12 @@ def test_sampled_accept_at_temperature_zero_is_greedy(name, vocab):
     ("tiny_p21_b8_h8", 512, 0.8, 0, 10.0),
     ("mixed_bs32_b16or32_h16", 32768, 1.0, 0, 11.5),
     ("mixed_bs32_b16or32_h16", 32768, 0.7, 20, 7.0),
+    # vocabularies that are not a multiple of 4: rows off the 16-byte grid
+    # (scalar loads) and row tails, with and without top-k
+    ("tiny_p21_b8_h8", 1001, 0.9, 0, 10.0),
+    ("tiny_p21_b8_h8", 1001, 0.9, 5, 8.0),
+    ("mixed_bs32_b16or32_h16", 20002, 1.0, 0, 11.5),
+    ("mixed_bs32_b16or32_h16", 20002, 0.8, 12, 7.0),
 ])
 def test_sampled_accept_matches_oracle(name, vocab, temp, top_k, bias):
     # probabilities are fp32 on the device and fp64 in the oracle: the seeds are
