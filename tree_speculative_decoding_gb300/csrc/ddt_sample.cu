@@ -111,6 +111,7 @@ struct SampleSmem {
     float step[kWarps][kMaxSteps];  // residual mass of each 256-id step of each warp's segment
     int removed[DDT_MAX_TOPK + 1];
     int nremoved;
+    unsigned gone[DDT_MAX_VOCAB / 32];  // the removed tokens as a bit set, for the bonus pass
     int decision;  // child taken, or -1
     float mass;
     int bonus;
@@ -194,7 +195,7 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
     return prefix;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict__ first_child,
                       const int32_t *__restrict__ next_sibling, const int32_t *__restrict__ qo_indptr,
                       const float *__restrict__ logits, int vocab, const float *__restrict__ temperature,
@@ -285,10 +286,12 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
             z = block_sum(part, sm);
         }
         // p(v) of the target at this node (0 outside the kept set), from its logit
+        const float inv_z = 1.f / z;
         auto prob_of = [&](int v, float x) -> float {
             if (v < 0 || v >= vocab) return 0.f;
             if (greedy) return v == amax ? 1.f : 0.f;
-            return order_key(x) >= thr ? __expf((x - lmax) * inv_t) / z : 0.f;
+            if (use_topk && order_key(x) < thr) return 0.f;
+            return __expf((x - lmax) * inv_t) * inv_z;
         };
         // the children against the residual (one thread, shared-memory values)
         if (tid == 0) {
@@ -330,10 +333,15 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         const int seg = ((vocab + kWarps - 1) / kWarps + 255) & ~255;
         const int s0 = warp * seg, s1 = min(vocab, s0 + seg);
         const int nsteps = s1 > s0 ? (s1 - s0 + 255) / 256 : 0;
+        for (int i = tid; i < (vocab + 31) >> 5; i += kThreads) sm.gone[i] = 0u;
+        __syncthreads();
+        if (tid < nrem) {
+            const int t = sm.removed[tid];
+            if (t >= 0 && t < vocab) atomicOr(&sm.gone[t >> 5], 1u << (t & 31));
+        }
+        __syncthreads();
         auto residual_of = [&](int v, float x) -> float {
-            bool gone = false;
-            for (int r = 0; r < nrem; ++r) gone |= sm.removed[r] == v;
-            return gone ? 0.f : prob_of(v, x);
+            return (sm.gone[v >> 5] >> (v & 31)) & 1u ? 0.f : prob_of(v, x);
         };
         // one step's lane-local running sums (loc), the lane total and its last id with mass
         auto step_sums = [&](int st, float (&loc)[8], float &lsum, int &llast) {
