@@ -108,7 +108,8 @@ struct SampleSmem {
     float fred[kWarps];
     int ired[kWarps];
     unsigned hist[256];
-    float step[kWarps][kMaxSteps];  // residual mass of each 256-id step of each warp's segment
+    float step[kWarps][kMaxSteps];  // mass of each 256-id step of each warp's segment
+    float stepmax[kWarps][kMaxSteps];  // the step's max logit (the temperature pass)
     int removed[DDT_MAX_TOPK + 1];
     int nremoved;
     unsigned gone[DDT_MAX_VOCAB / 32];  // the removed tokens as a bit set, for the bonus pass
@@ -227,6 +228,15 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         sm.fc[i] = first_child[base + i];
         sm.ns[i] = next_sibling[base + i];
     }
+    // warp w owns ids [w * seg, (w + 1) * seg) in steps of 256 ids, lane l
+    // holding ids [8l, 8l+8) of a step
+    const int warp = tid >> 5, lane = tid & 31;
+    const int seg = ((vocab + kWarps - 1) / kWarps + 255) & ~255;
+    const int s0 = warp * seg, s1 = min(vocab, s0 + seg);
+    const int nsteps = s1 > s0 ? (s1 - s0 + 255) / 256 : 0;
+    // at temperature > 0 without top-k the first pass also keeps, per step, the
+    // sum of e^{(x - m)/T} and its max m, so the bonus draw needs no second pass
+    const bool step_pass = !greedy && !use_topk;
     int cur = 0, n = 1;
     if (tid == 0) path[0] = 0;
     int bon = -1;
@@ -258,25 +268,58 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
             sm.kid_coin[tid] = u[tid];
             prefetch_row(logits + (size_t)(base + sm.kid[tid]) * vocab, vocab);  // the next level's candidates
         }
-        // the argmax, the max logit and (without top-k) the normaliser, in one
-        // online pass: sum e^{(x - m)/T} with m the running max of this thread
-        float lv = -INFINITY, ls = 0.f;
+        // the argmax and the max logit; at temperature > 0 also the normaliser
+        float lv = -INFINITY;
         int li = vocab;
-        for_each_logit(row, vocab, [&](int v, float x) {
-            if (x > lv || (x == lv && v < li)) {
-                if (!greedy && x > lv) ls = (lv == -INFINITY ? 0.f : ls * __expf((lv - x) * inv_t));
-                lv = x;
-                li = v;
+        if (step_pass) {
+            for (int st = 0; st < nsteps; ++st) {
+                const int b0 = s0 + 256 * st + 8 * lane;
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[k] = b0 + k < s1 ? row[b0 + k] : -INFINITY;
+                float m = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (b0 + k < s1 && (x[k] > lv || (x[k] == lv && b0 + k < li))) {
+                        lv = x[k];
+                        li = b0 + k;
+                    }
+                    m = fmaxf(m, x[k]);
+                }
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+                float e = 0.f;
+                if (m != -INFINITY) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) e += __expf((x[k] - m) * inv_t);
+                }
+                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(FULL, e, o);
+                if (lane == 0) {
+                    sm.step[warp][st] = e;
+                    sm.stepmax[warp][st] = m;
+                }
             }
-            if (!greedy && !use_topk) ls += __expf((x - lv) * inv_t);
-        });
+        } else {
+            for_each_logit(row, vocab, [&](int v, float x) {
+                if (x > lv || (x == lv && v < li)) {
+                    lv = x;
+                    li = v;
+                }
+            });
+        }
         float lmax;
         int amax;
-        block_argmax(lv, li, sm, lmax, amax);
+        block_argmax(lv, li, sm, lmax, amax);  // (its barriers publish the step sums)
         unsigned thr = 0;
         float z = 1.f;
-        if (!greedy && !use_topk) {
-            z = block_sum(lv == -INFINITY ? 0.f : ls * __expf((lv - lmax) * inv_t), sm);
+        if (step_pass) {  // the step sums rescaled to lmax; z is their total
+            float part = 0.f;
+            for (int st = lane; st < nsteps; st += 32) {
+                const float m = sm.stepmax[warp][st];
+                const float e = m == -INFINITY ? 0.f : sm.step[warp][st] * __expf((m - lmax) * inv_t);
+                sm.step[warp][st] = e;
+                part += e;
+            }
+            z = block_sum(part, sm);
         } else if (use_topk) {  // kept set first, then the normaliser over it
             thr = kth_largest_key(row, vocab, kk, sm);
             float part = 0.f;
@@ -327,13 +370,9 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         }
         const int nrem = sm.nremoved;
         const float target = u[coin_stride - 1] * sm.mass;
-        const int warp = tid >> 5, lane = tid & 31;
-        // warp w owns ids [w * seg, (w + 1) * seg) in steps of 256 ids, lane l
-        // holding ids [8l, 8l+8) of a step; each step's residual mass is kept
-        const int seg = ((vocab + kWarps - 1) / kWarps + 255) & ~255;
-        const int s0 = warp * seg, s1 = min(vocab, s0 + seg);
-        const int nsteps = s1 > s0 ? (s1 - s0 + 255) / 256 : 0;
         for (int i = tid; i < (vocab + 31) >> 5; i += kThreads) sm.gone[i] = 0u;
+        if (step_pass)  // step masses as probabilities
+            for (int st = lane; st < nsteps; st += 32) sm.step[warp][st] *= inv_z;
         __syncthreads();
         if (tid < nrem) {
             const int t = sm.removed[tid];
@@ -343,93 +382,116 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         auto residual_of = [&](int v, float x) -> float {
             return (sm.gone[v >> 5] >> (v & 31)) & 1u ? 0.f : prob_of(v, x);
         };
-        // one step's lane-local running sums (loc), the lane total and its last id with mass
-        auto step_sums = [&](int st, float (&loc)[8], float &lsum, int &llast) {
-            const int b0 = s0 + 256 * st + 8 * lane;
+        // step st of warp w's segment, per element: this lane's running sums (loc),
+        // its total and its last id with mass
+        auto step_sums = [&](int w, int st, float (&loc)[8], float &lsum, int &llast) {
+            const int w1 = min(vocab, w * seg + seg);
+            const int b0 = w * seg + 256 * st + 8 * lane;
             float x[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = b0 + k < s1 ? row[b0 + k] : 0.f;
+            for (int k = 0; k < 8; ++k) x[k] = b0 + k < w1 ? row[b0 + k] : 0.f;
             lsum = 0.f;
             llast = -1;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float pv = b0 + k < s1 ? residual_of(b0 + k, x[k]) : 0.f;
+                const float pv = b0 + k < w1 ? residual_of(b0 + k, x[k]) : 0.f;
                 lsum += pv;
                 loc[k] = lsum;
                 if (pv > 0.f) llast = b0 + k;
             }
         };
-        int wlast = -1;
-        for (int st = 0; st < nsteps; ++st) {
-            float loc[8], lsum;
-            int llast;
-            step_sums(st, loc, lsum, llast);
-            for (int o = 16; o > 0; o >>= 1) {
-                lsum += __shfl_xor_sync(FULL, lsum, o);
-                llast = max(llast, __shfl_xor_sync(FULL, llast, o));
+        auto warp_total = [&](float lsum) {
+            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(FULL, lsum, o);
+            return lsum;
+        };
+        if (step_pass) {
+            // only the steps holding a removed token change: warp j recomputes the
+            // step of removed token j per element, once per step (steps are the
+            // id blocks [256i, 256i + 256), since seg is a multiple of 256)
+            for (int j = warp; j < nrem; j += kWarps) {
+                const int t = sm.removed[j];
+                bool first = t >= 0 && t < vocab;
+                for (int r = 0; r < j && first; ++r) {
+                    const int q = sm.removed[r];
+                    if (q >= 0 && q < vocab && q >> 8 == t >> 8) first = false;
+                }
+                if (first) {
+                    const int w = t / seg, st = (t - w * seg) >> 8;
+                    float loc[8], lsum;
+                    int llast;
+                    step_sums(w, st, loc, lsum, llast);
+                    lsum = warp_total(lsum);
+                    if (lane == 0) sm.step[w][st] = lsum;
+                }
             }
-            if (lane == 0) sm.step[warp][st] = lsum;
-            wlast = max(wlast, llast);
+        } else {  // top-k: every step per element
+            for (int st = 0; st < nsteps; ++st) {
+                float loc[8], lsum;
+                int llast;
+                step_sums(warp, st, loc, lsum, llast);
+                lsum = warp_total(lsum);
+                if (lane == 0) sm.step[warp][st] = lsum;
+            }
         }
-        if (lane == 0) sm.ired[warp] = wlast;
-        if (tid == 0) sm.bonus = -1;
         __syncthreads();
-        // the crossing step: running prefixes over (warp, step) in id order, the same
-        // numbers in every thread, so at most one step qualifies
+        // warp 0: the crossing step from running prefixes over (warp, step) in id
+        // order (the same numbers in every lane), or, if rounding left the target
+        // above the total, the last step with mass; then that step per element
         if (warp == 0) {
-            float pre = 0.f;
-            int cw = -1, cs = -1;
-            float cpre = 0.f;
+            float pre = 0.f, cpre = 0.f, lpre = 0.f;
+            int cw = -1, cs = -1, lw = -1, ls = -1;
             for (int w = 0; w < kWarps && cw < 0; ++w) {
                 const int ws0 = w * seg, ws1 = min(vocab, ws0 + seg);
                 const int wn = ws1 > ws0 ? (ws1 - ws0 + 255) / 256 : 0;
                 for (int st = 0; st < wn; ++st) {
-                    const float nxt = pre + sm.step[w][st];
+                    const float mass_s = sm.step[w][st];
+                    const float nxt = pre + mass_s;
                     if (pre <= target && target < nxt) {
                         cw = w;
                         cs = st;
                         cpre = pre;
                         break;
                     }
+                    if (mass_s > 0.f) {
+                        lw = w;
+                        ls = st;
+                        lpre = pre;
+                    }
                     pre = nxt;
                 }
             }
-            if (lane == 0) {  // scratch: the crossing warp, its step and the prefix before it
-                sm.decision = cw;
-                sm.mass = cpre;
-                sm.nkid = cs;
+            if (cw < 0) {
+                cw = lw;
+                cs = ls;
+                cpre = lpre;
             }
-        }
-        __syncthreads();
-        if (sm.decision == warp) {  // the crossing warp scans its one crossing step
-            float loc[8], lsum;
-            int llast;
-            step_sums(sm.nkid, loc, lsum, llast);
-            float incl = lsum;
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(FULL, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const float base_l = sm.mass + incl - lsum;  // this lane's prefix
-            const int b0 = s0 + 256 * sm.nkid + 8 * lane;
-            int mine = -1;  // the lane's first id with mass whose running sum passes the target
-            if (base_l + lsum > target)
-#pragma unroll
-                for (int k = 7; k >= 0; --k) {
-                    const bool mass_k = k == 0 ? loc[0] > 0.f : loc[k] > loc[k - 1];
-                    if (b0 + k < s1 && mass_k && base_l + loc[k] > target) mine = b0 + k;
+            int pick = amax;  // no residual mass at all
+            if (cw >= 0) {
+                float loc[8], lsum;
+                int llast;
+                step_sums(cw, cs, loc, lsum, llast);
+                float incl = lsum;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += y;
                 }
-            const unsigned hit = __ballot_sync(FULL, mine >= 0);
-            int lastw = llast;
-            for (int o = 16; o > 0; o >>= 1) lastw = max(lastw, __shfl_xor_sync(FULL, lastw, o));
-            const int first = __shfl_sync(FULL, mine, hit ? __ffs(hit) - 1 : 0);
-            if (lane == 0) sm.bonus = hit ? first : lastw;  // rounding: the step's last id with mass
-        }
-        __syncthreads();
-        if (tid == 0 && sm.bonus < 0) {  // rounding put the target above the total
-            int best = -1;
-            for (int w = 0; w < kWarps; ++w) best = max(best, sm.ired[w]);
-            sm.bonus = best >= 0 ? best : amax;
+                const float base_l = cpre + incl - lsum;  // this lane's prefix
+                const int b0 = cw * seg + 256 * cs + 8 * lane;
+                const int w1 = min(vocab, cw * seg + seg);
+                int mine = -1;  // the lane's first id with mass whose running sum passes the target
+                if (base_l + lsum > target)
+#pragma unroll
+                    for (int k = 7; k >= 0; --k) {
+                        const bool mass_k = k == 0 ? loc[0] > 0.f : loc[k] > loc[k - 1];
+                        if (b0 + k < w1 && mass_k && base_l + loc[k] > target) mine = b0 + k;
+                    }
+                const unsigned hit = __ballot_sync(FULL, mine >= 0);
+                int lastw = llast;
+                for (int o = 16; o > 0; o >>= 1) lastw = max(lastw, __shfl_xor_sync(FULL, lastw, o));
+                const int first = __shfl_sync(FULL, mine, hit ? __ffs(hit) - 1 : 0);
+                pick = hit ? first : (lastw >= 0 ? lastw : amax);  // rounding: the step's last id with mass
+            }
+            if (lane == 0) sm.bonus = pick;
         }
         __syncthreads();
         bon = sm.bonus;
