@@ -322,7 +322,9 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
  * Every emitted token is then distributed as p.  At temperature 0 (or top_k
  * 1) this is exactly ddt_accept with target_argmax = the logits' argmax.
  * Probabilities are fp32 on the device, so a coin within ~1e-6 of a threshold
- * may decide differently from an fp64 evaluation.
+ * may decide differently from an fp64 evaluation.  If rounding leaves the
+ * bonus target at or above the residual's total, the bonus is a token with
+ * residual mass near the end of the id range (the argmax if r is empty).
  *
  *   node_token, first_child, next_sibling, qo_indptr
  *                 (device) the tree (ddt_build_tree) and its links (ddt_tree_links).
@@ -333,9 +335,9 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
  *                 bonus; coin_stride >= 1 + the largest number of children.
  *   outputs       as for ddt_accept.
  * Supported: 1 <= vocab <= DDT_MAX_VOCAB.
- * Device checks: links that do not form the tree or a node with more
- * children than coin_stride - 1 (DDT_DEVERR_SAMPLE; outputs unset), a walk
- * deeper than max_depth (DDT_DEVERR_DEPTH).
+ * Device checks: links that do not form the tree, or a node with more
+ * children than coin_stride - 1 or than DDT_MAX_TOPK + 1 (DDT_DEVERR_SAMPLE;
+ * outputs unset), a walk deeper than max_depth (DDT_DEVERR_DEPTH).
  */
 ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_child,
                               const int32_t *next_sibling, const int32_t *qo_indptr,
