@@ -162,6 +162,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(wl):
+    """The workload's shape, as both arms report it."""
+    return {"workload": wl.name, "batch": wl.B, "heads": wl.H, "prefix": int(wl.prefix_len[0]),
+            "budget": int(wl.budget[0]), "q_len": int(wl.q_len[0]), "topk": wl.K,
+            "pool_rows": wl.pool_rows}
+
+
 def run_device(args, rank, world, local_rank):
     import torch
 
@@ -290,12 +297,10 @@ def run_device(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; N(0,1) bf16 q and latent KV; drafter top-k from "
                 "log-softmax of N(0,3) logits)",
-        "config": {"workload": wl.name, "batch": wl.B, "heads": wl.H, "prefix": int(wl.prefix_len[0]),
-                   "budget": int(wl.budget[0]), "q_len": int(wl.q_len[0]), "topk": wl.K,
-                   "pool_rows": wl.pool_rows, "num_splits": st.num_splits,
-                   "l2": "flushed (256 MiB write) before every timed step",
-                   "timing": "CUDA graph replay of the 4-stage step, CUDA events per step",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(workload_config(wl), num_splits=st.num_splits,
+                       l2="flushed (256 MiB write) before every timed step",
+                       timing="CUDA graph replay of the 4-stage step, CUDA events per step",
+                       parallelism=f"replicas x{world}"),
         "kv_gbs": round(kvb * args.steps * world / elapsed_max / 1e9, 2),
         "steps_per_s": round(args.steps * world / elapsed_max, 1),
         "attn_flops_per_step": flops,
@@ -557,7 +562,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": dict(workload_config(wl), timing="host wall clock per oracle step",
+                           parallelism="rank 0 only"),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
                              "cores": oracle.num_threads(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

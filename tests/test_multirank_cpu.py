@@ -43,3 +43,23 @@ def test_two_rank_reduction():
 def test_single_rank_is_identity():
     import bench
     assert bench.reduce_over_ranks(3.0, 7.0, None) == (3.0, 7.0)
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    # the reference arm is the CPU oracle: it runs here, on a bounded sample per step
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["value"] > 0
+    assert line["config"]["workload"] == bench.WORKLOAD and line["config"]["heads"] == 64
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_bench_rejects_fewer_than_three_warmup_steps():
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--steps", "1", "--warmup", "2"])
