@@ -505,15 +505,16 @@ def step_timeline(workload, reps=50):
     return {"workload": workload, "num_splits": st.num_splits, "kernels": out}
 
 
-def oracle_step(wl, rows=None):
-    """One verify step of the CPU oracle; returns attention FLOPs of the rows it computed."""
+def oracle_step(wl, rows=None, nthreads=0):
+    """One verify step of the CPU oracle (attention on `nthreads` threads, 0 = all);
+    returns attention FLOPs of the rows it computed."""
     import oracle
     from tree_speculative_decoding_gb300.metrics import attn_flops
     tok, par, dep = oracle.build_tree(wl.topk_logp, wl.topk_ids, wl.root_id, wl.budget,
                                       wl.qo_indptr, wl.max_depth, wl.K)
     mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
     oracle.verify_attn(wl.q, wl.kv_pool, wl.kv_indices, wl.kv_indptr, wl.qo_indptr, mask, mip,
-                       wl.H, wl.scale, rows=rows)
+                       wl.H, wl.scale, rows=rows, nthreads=nthreads)
     oracle.accept(tok, par, wl.qo_indptr, wl.argmax_random, wl.max_depth)
     full = attn_flops(wl.prefix_len, dep, wl.qo_indptr, wl.H)
     if rows is None:
@@ -524,6 +525,7 @@ def oracle_step(wl, rows=None):
 def cpu_baseline(wl, seconds=10.0):
     import oracle
     oracle.build()
+    cores = oracle.num_threads()
     total, t0, reps = 0.0, time.perf_counter(), 0
     while True:
         total += oracle_step(wl)
@@ -531,10 +533,18 @@ def cpu_baseline(wl, seconds=10.0):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(total / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    # the same on one thread, over a bounded sample of rows
+    rows = np.arange(min(256, wl.total_q * wl.H), dtype=np.int64)
+    t1 = time.perf_counter()
+    f1 = oracle_step(wl, rows, nthreads=1)
+    d1 = time.perf_counter() - t1
+    return {"value": round(total / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} full oracle verify steps of {wl.name} (tree, mask, fp64 attention "
-                      f"over all {wl.total_q * wl.H} rows, accept) in {dt:.1f} s"}
+                      f"over all {wl.total_q * wl.H} rows, accept) in {dt:.1f} s",
+            "single_thread": {"value": round(f1 / d1 / 1e12, 6), "cores": 1,
+                              "sample": f"one oracle step with fp64 attention for {len(rows)} of "
+                                        f"{wl.total_q * wl.H} rows in {d1:.2f} s"}}
 
 
 def run_reference(args, rank, world):

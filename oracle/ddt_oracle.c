@@ -290,13 +290,16 @@ int oracle_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_
             if (s < 0 || s >= pool_rows) return OR_ERR_ARG;
         }
     }
+    /* the thread count for this call only (0: all of OpenMP's default) */
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    int team = nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
+    int team = 1;
     (void)nthreads;
 #endif
+    (void)team;
 
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(team)
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t t = rows[r] / H;
         int h = (int)(rows[r] % H);

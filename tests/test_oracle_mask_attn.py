@@ -194,3 +194,17 @@ def test_ragged_batch_rows_match_single_request_calls(oracle_mod):
                                     b["mip"], 2, 0.14468)
     np.testing.assert_array_equal(out, np.concatenate([oa, ob]))
     np.testing.assert_array_equal(lse, np.concatenate([la, lb]))
+
+
+def test_thread_count_is_per_call(oracle_mod):
+    # rows are independent, so one thread and all threads give the same bits; a
+    # one-thread call leaves the default team size of later calls unchanged
+    c = _tiny_case(oracle_mod, 8, 40, 3, 3, 12, H=8)
+    before = oracle_mod.num_threads()
+    one = oracle_mod.verify_attn(c["q"], c["pool"], c["slots"], c["kvp"], c["qo"], c["mask"],
+                                 c["mip"], c["H"], 0.2, nthreads=1)
+    assert oracle_mod.num_threads() == before
+    every = oracle_mod.verify_attn(c["q"], c["pool"], c["slots"], c["kvp"], c["qo"], c["mask"],
+                                   c["mip"], c["H"], 0.2)
+    for a, b in zip(one, every):
+        assert np.array_equal(a, b)
