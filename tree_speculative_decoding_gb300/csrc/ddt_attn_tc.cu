@@ -27,7 +27,7 @@
 //     pair swaps fp32 partials through distributed shared memory: CTA c owns
 //     the softmax of rows [64c, 64c+64).  The owner adds the two partials,
 //     applies the mask, runs the online softmax (the running max moves only
-//     when a block max exceeds it by more than 2^20), writes P (bf16) locally
+//     when a block max exceeds it by more than 2^48), writes P (bf16) locally
 //     and bulk-copies its rows to the partner with the rows' rescale factors.
 //     Each CTA then accumulates O_c += P V_c (tcgen05.mma, M=128, N=256, K=64,
 //     V read as an MN-major operand straight from the gathered stage).  P and
