@@ -80,6 +80,46 @@ def test_num_splits_is_bounded(lib):
         assert s == 1 or N // s >= 64
 
 
+def _wave_model(B, H, T, N, sms):
+    """The split choice as documented: one split for a batch that fills half the
+    SMs with row tiles; else the count (>= 4 kv blocks of 64 per split) with the
+    fewest waves x (blocks per split + 8), ties to fewer splits."""
+    tiles = B * -(-(T * H) // 128)
+    pairs = max(sms // 2, 1)
+    if B > 1 and tiles >= pairs:
+        return 1
+    blocks = -(-N // 64)
+    best, best_cost = 1, None
+    for s in range(1, max(1, min(blocks // 4, 128)) + 1):
+        cost = -(-(tiles * s) // pairs) * (-(-blocks // s) + 8)
+        if best_cost is None or cost < best_cost:
+            best, best_cost = s, cost
+    return best
+
+
+def test_split_choice_for_the_timed_shapes(lib):
+    # (batch, heads, max q_len, max kv_len) -> splits on 152 SMs
+    cases = {(1, 64, 33, 4129): 4,        # one request, prefix 4096, budget 32
+             (1, 64, 65, 131137): 9,      # long context
+             (8, 64, 33, 16417): 1,       # ragged batch: the row tiles fill the SMs
+             (32, 16, 33, 8225): 1,       # mixed batch of 32
+             (1, 64, 1, 4097): 13,        # autoregressive step
+             (1, 64, 128, 4224): 1}       # prefill chunk of 128 tokens
+    for (B, H, T, N), want in cases.items():
+        assert lib.ddt_verify_attn_num_splits(B, H, T, N, 152) == want, (B, H, T, N)
+
+
+def test_split_choice_follows_the_wave_model(lib):
+    rng = __import__("numpy").random.default_rng(0)
+    for _ in range(300):
+        B = int(rng.choice([1, 1, 2, 3, 8, 40]))
+        H = int(rng.choice([1, 8, 16, 64, 128]))
+        T = int(rng.integers(1, 129))
+        N = T + int(rng.integers(0, 300000))
+        sms = int(rng.choice([148, 152, 20]))
+        assert lib.ddt_verify_attn_num_splits(B, H, T, N, sms) == _wave_model(B, H, T, N, sms)
+
+
 def test_host_argument_checks_launch_nothing(lib):
     dummy = ctypes.c_void_p(16)
     # null pointers -> invalid argument, returned before any CUDA call
