@@ -578,3 +578,75 @@ def test_sampled_accept_emits_the_target_distribution():
     freq = np.bincount(first, minlength=V) / B
     assert np.abs(freq - p).max() < 4.5 * np.sqrt(0.25 / B)
 
+
+
+@pytest.mark.parametrize("top_k", [0, 64])
+def test_sampled_accept_at_the_largest_vocabulary(top_k):
+    # vocab 262144 (the ABI's bound), a sharp temperature: each warp's segment
+    # spans 64 steps of 256 ids.  The seed is one whose decisions do not move
+    # when every coin moves by 3e-5, so fp32 and fp64 must agree.
+    wl = workloads.preset("tiny_p21_b8_h8")
+    st, tok, par, logits, coins = _sampling_case(wl, 262144, 16, 8.0)
+    t = np.full(wl.B, 0.35)
+    k = np.full(wl.B, top_k)
+    got = _sampled(st, logits, t, k, coins)
+    ref = oracle.accept_sampled(tok, par, wl.qo_indptr, logits, t, k, coins, wl.max_depth)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+    assert got[0].max() > 1
+
+
+def test_sampled_accept_residual_draw_over_many_steps():
+    # 4096 copies of one root with three leaf children whose tokens sit in
+    # different 256-id steps of a 4096-id vocabulary; the first emitted token
+    # must follow p(root), checked per step and on the five likeliest tokens
+    from tree_speculative_decoding_gb300 import ddt
+    B, V, temp = 4096, 4096, 0.8
+    rng = np.random.default_rng(21)
+    l = rng.normal(scale=1.0, size=V).astype(np.float32)
+    l[rng.choice(V, 24, replace=False)] += 4.0          # some mass in a few tokens
+    kids = np.array([100, 1500, 3900], np.int32)
+    l[kids] += 3.0
+    p = np.exp((l.astype(np.float64) - l.max()) / temp)
+    p /= p.sum()
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), B)
+    tok = np.tile(np.concatenate([[7], kids]).astype(np.int32), B)
+    qo = np.arange(B + 1, dtype=np.int32) * 4
+    fc = np.tile(np.array([1, -1, -1, -1], np.int32), B)
+    ns = np.tile(np.array([-1, 2, 3, -1], np.int32), B)
+    logits = np.tile(l, (B * 4, 1))
+    coins = rng.random((B * 4, 4)).astype(np.float32)
+    d = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
+    out = [torch.empty(B, dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty(B, dtype=torch.int32, device="cuda:0")]
+    ddt.ddt_accept_sampled(d(tok, np.int32), d(fc, np.int32), d(ns, np.int32), d(qo, np.int32),
+                           d(logits, np.float32), d(np.full(B, temp), np.float32),
+                           d(np.zeros(B), np.int32), d(coins, np.float32), 2, *out)
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (0, 0)
+    first = out[2][:, 0].cpu().numpy()
+    freq = np.bincount(first, minlength=V) / B
+    f_step, p_step = freq.reshape(16, 256).sum(1), p.reshape(16, 256).sum(1)
+    assert np.all(np.abs(f_step - p_step) < 4.5 * np.sqrt(p_step * (1 - p_step) / B) + 1e-3)
+    top = np.argsort(p)[::-1][:5]
+    assert np.all(np.abs(freq[top] - p[top]) < 4.5 * np.sqrt(p[top] * (1 - p[top]) / B) + 1e-3)
+
+
+def test_sampled_accept_latches_too_few_coins():
+    # a root with three children but coins for two: a device check, no fault
+    from tree_speculative_decoding_gb300 import ddt
+    d = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
+    out = [torch.full((1,), -7, dtype=torch.int32, device="cuda:0"),
+           torch.empty((1, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty((1, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty(1, dtype=torch.int32, device="cuda:0")]
+    assert ddt.ddt_get_error() == (0, 0)
+    ddt.ddt_accept_sampled(d([0, 1, 2, 3], np.int32), d([1, -1, -1, -1], np.int32),
+                           d([-1, 2, 3, -1], np.int32), d([0, 4], np.int32),
+                           d(np.zeros((4, 16)), np.float32), d([1.0], np.float32),
+                           d([0], np.int32), d(np.full((4, 3), 0.5), np.float32), 2, *out)
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (5, 0x400)
+    assert out[0].item() == -7                            # outputs left unset
