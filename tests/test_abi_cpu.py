@@ -144,6 +144,20 @@ def test_host_argument_checks_launch_nothing(lib):
                                   None) == 1   # vocab 0
     assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 3, 1, 8, dummy, dummy, dummy,
                                   dummy, None) == 2  # max_depth 8
+    assert lib.ddt_accept_sampled(*sa, 262145, dummy, dummy, dummy, 3, 1, 7, dummy, dummy, dummy,
+                                  dummy, None) == 2  # vocab above DDT_MAX_VOCAB
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 0, 1, 7, dummy, dummy, dummy,
+                                  dummy, None) == 1  # no coins
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 3, 0, 7, dummy, dummy, dummy,
+                                  dummy, None) == 0  # empty batch: nothing to do
+    # the allocation-free attention makes the same host checks before touching the device
+    na = [dummy, dummy, 100, dummy, dummy, dummy, dummy, dummy]
+    assert lib.ddt_verify_attn_noalloc(*na, 1, 8, 9, 9, 30, 0.1, 0, None, None, None) == 1
+    assert lib.ddt_verify_attn_noalloc(*na, 1, 8, 9, 9, 30, 0.1, 129, dummy, None, None) == 2
+    assert lib.ddt_verify_attn_noalloc(*na, 1, 8, 9, 9, 30, 0.1, -1, dummy, None, None) == 1
+    assert lib.ddt_verify_attn_noalloc(*na, 1, 129, 9, 9, 30, 0.1, 0, dummy, None, None) == 2
+    assert lib.ddt_verify_attn_noalloc(dummy, ctypes.c_void_p(18), *na[2:], 1, 8, 9, 9, 30, 0.1,
+                                       0, dummy, None, None) == 1   # misaligned kv_pool
     assert lib.ddt_verify_step(None, None) == 1
     assert lib.ddt_step_graph_create(None, None) == 1
     assert lib.ddt_step_graph_launch(None, None) == 1
