@@ -73,14 +73,15 @@ def test_noalloc_rejects_scratch_beyond_its_capacity(step):
 
 
 def test_noalloc_own_split_choice_fits_its_scratch():
-    # one request, prefix 32768, budget 64, 64 heads: the split count the
-    # workspace entry point picks needs more than the fixed scratch, so the
-    # allocation-free call must pick a smaller one rather than refuse
+    # one request, prefix 16384, budget 96, 64 heads (6208 rows): the split
+    # count the workspace entry point picks (3 or more for any SM count from
+    # 132 to 160) needs more than the fixed scratch, so the allocation-free
+    # call must pick a smaller one rather than refuse
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from tree_speculative_decoding_gb300 import ddt
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
-    wl = workloads.make_workload("noalloc_long", 0xA110D, 1, 64, [32768], [64], 8, 32768, 3.0)
+    wl = workloads.make_workload("noalloc_long", 0xA110D, 1, 64, [16384], [96], 8, 32768, 3.0)
     st = VerifyStep(wl, "cuda:0")
     st.run()
     torch.cuda.synchronize()
