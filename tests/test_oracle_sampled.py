@@ -141,3 +141,64 @@ def test_more_children_than_coins_is_rejected(oracle_mod):
         oracle_mod.accept_sampled(tok, par, np.array([0, 4], np.int32),
                                   np.zeros((4, 5), np.float32), np.array([1.0], np.float32),
                                   np.array([0], np.int32), np.full((4, 3), 0.99, np.float32), 3)
+
+
+def _deep_case(seed, V=40, T_bias=6.0):
+    tok, par, dep, _ = _tree(seed)
+    T = len(tok)
+    rng = np.random.default_rng(200 + seed)
+    logits = rng.normal(size=(T, V)).astype(np.float32)
+    for n in range(T):
+        kids = [c for c in range(1, T) if par[c] == n]
+        if kids:
+            logits[n, tok[kids[0]]] += T_bias
+    coins = rng.random((T, 4)).astype(np.float32)
+    return tok, par, np.array([0, T], np.int32), logits, coins
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_a_constant_added_to_the_logits_changes_nothing(oracle_mod, seed):
+    # softmax is shift invariant; +8 is exact in fp32 for these magnitudes
+    tok, par, qo, logits, coins = _deep_case(seed)
+    t, k = np.array([0.9], np.float32), np.array([0], np.int32)
+    a = oracle_mod.accept_sampled(tok, par, qo, logits, t, k, coins, 4)
+    b = oracle_mod.accept_sampled(tok, par, qo, logits + np.float32(8.0), t, k, coins, 4)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_top_k_of_the_whole_vocabulary_is_no_top_k(oracle_mod, seed):
+    tok, par, qo, logits, coins = _deep_case(seed)
+    t = np.array([1.1], np.float32)
+    a = oracle_mod.accept_sampled(tok, par, qo, logits, t, np.array([0], np.int32), coins, 4)
+    b = oracle_mod.accept_sampled(tok, par, qo, logits, t, np.array([40], np.int32), coins, 4)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_a_vanishing_temperature_is_the_greedy_walk(oracle_mod, seed):
+    # with distinct logits, T -> 0 puts all mass on the argmax
+    tok, par, qo, logits, coins = _deep_case(seed)
+    a = oracle_mod.accept_sampled(tok, par, qo, logits, np.array([1e-3], np.float32),
+                                  np.array([0], np.int32), coins, 4)
+    g = oracle_mod.accept(tok, par, qo, logits.argmax(axis=1).astype(np.int32), 4)
+    for x, y in zip(a, g):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_a_one_token_vocabulary_accepts_the_matching_child(oracle_mod):
+    # p = 1 on token 0: the child carrying token 0 is always taken (coin < 1),
+    # any child before it is rejected with zero mass removed, and the bonus is 0
+    par = np.array([-1, 0, 0, 2], np.int32)
+    tok = np.array([5, 3, 0, 0], np.int32)
+    coins = np.full((4, 4), 0.999, np.float32)
+    alen, acc, com, bon = oracle_mod.accept_sampled(tok, par, np.array([0, 4], np.int32),
+                                                    np.zeros((4, 1), np.float32),
+                                                    np.array([1.0], np.float32),
+                                                    np.array([0], np.int32), coins, 3)
+    assert alen.tolist() == [3]
+    assert acc[0].tolist() == [0, 2, 3, -1]
+    assert com[0].tolist() == [0, 0, 0, -1]
+    assert bon.tolist() == [0]
