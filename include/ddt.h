@@ -1,7 +1,7 @@
 /*
  * ddt.h -- C ABI of the GB300 (sm_103a) DDTree verify step.
  *
- * Four stages of one speculative-decoding verify step, as defined on the pages
+ * The stages of one speculative-decoding verify step, as defined on the pages
  * "The DDTree CUDA Graph Fix: Unlocking Speculative Decoding at 109 tok/s on
  * PCIe Blackwell" (section "The DDTree Architecture: Confirming Multiple-Path
  * Evaluation"), "The Architecture of a Speculative Decoding Engine" (sections
@@ -11,17 +11,23 @@
  *
  *   ddt_build_tree          best-first expansion of per-depth top-k log-probs
  *   ddt_compile_visibility  bit-packed [q_len, prefix + q_len] visibility mask
+ *   ddt_build_tree_visibility  the two above in one launch
  *   ddt_verify_attn         tree-verify MLA attention in absorbed form
+ *                           (ddt_verify_attn_noalloc: without a caller workspace)
  *   ddt_accept              greedy walk: longest accepted chain + bonus token
  *   ddt_commit_kv           gather the accepted latents after the committed prefix
  *   ddt_tree_links          the tree as first-child / next-sibling links
  *   ddt_accept_sampled      tree rejection sampling with temperature and top-k
+ *   ddt_verify_step         tree + mask, attention, accept (+ commit) in one call;
+ *                           ddt_step_graph_* hold the same as one CUDA graph
  *
  * Conventions for every entry point:
  *   - Pointers marked (device) must be device memory of the current CUDA
  *     device; pointers marked (host) are host memory.  The caller owns all
  *     memory.  No entry point allocates device memory; split-KV scratch is a
- *     caller-provided workspace sized by ddt_verify_attn_workspace_size().
+ *     caller-provided workspace sized by ddt_verify_attn_workspace_size()
+ *     (ddt_verify_attn_noalloc uses a fixed array inside the library, and an
+ *     instantiated step graph holds CUDA's own graph resources).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Launches are
  *     asynchronous on that stream; no entry point synchronises the host except
  *     ddt_get_error().
@@ -30,8 +36,9 @@
  *     kernel waits for that kernel before it reads anything that an earlier
  *     stage of this ABI writes (tree, mask, split partials) and before its
  *     first write.  Arguments that only the caller writes (q, kv_pool,
- *     kv_indices, the indptr arrays, top-k inputs, target_argmax) are read
- *     before that wait.  Producing them in a kernel that signals early
+ *     kv_indices, the indptr arrays, top-k inputs, target_argmax, and the
+ *     sampling accept's temperature, top_k and logits) may be read before
+ *     that wait.  Producing them in a kernel that signals early
  *     completion (cudaTriggerProgrammaticLaunchCompletion) and then calling
  *     an entry point right after it is therefore unsupported.  An ordinary
  *     kernel, a copy or an event between the producer and the call is
