@@ -42,8 +42,9 @@ if ROOT not in sys.path:
 WORKLOAD = "single_p4096_b32_h64"
 METRIC = "verify-attn TFLOP/s and KV GB/s per step, % of roofline, 1xGB300"
 # DRAM bytes (read + write) of one ddt_verify_attn call (partial + combine kernels) on
-# this workload, from ncu (profiles/attn_tc_single_p4096_b32_h64.md), valid only for the
-# kernel sources it was taken from: a change to them turns the field back to null.
+# this workload, from an ncu capture of both kernels (dram__bytes_read.sum +
+# dram__bytes_write.sum per launch); valid only for the kernel sources it was taken
+# from (their digests below): a change to them turns the field back to null.
 PROFILE_TRAFFIC = {
     "bytes": 7293184 + 0 + 17346560 + 0,
     "sources": {
@@ -192,12 +193,14 @@ def run_device(args, rank, world, local_rank):
     flops = attn_flops(wl.prefix_len, depth, wl.qo_indptr, wl.H)
     kvb = kv_bytes(wl.kv_indptr)
 
+    # the step is the one-call C-ABI step (ddt_verify_step): tree + mask,
+    # attention, accept, captured once and replayed
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
-            st.run(stream=stream)
+            st.run_one_call(stream=stream)
     torch.cuda.synchronize()
 
     # kernels launched per step: tree + mask (one launch), attention partial (+ combine), accept
@@ -297,7 +300,7 @@ def run_device(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; N(0,1) bf16 q and latent KV; drafter top-k from "
                 "log-softmax of N(0,3) logits)",
-        "config": dict(workload_config(wl), num_splits=st.num_splits,
+        "config": dict(workload_config(wl), num_splits=st.launched_splits,
                        l2="flushed (256 MiB write) before every timed step",
                        timing="CUDA graph replay of the 4-stage step, CUDA events per step",
                        parallelism=f"replicas x{world}"),
@@ -431,7 +434,7 @@ def time_degenerate(dev, stream, flush, reps=200):
                 st.verify_attn(stream=s)
         else:
             def body(s, st=st):
-                st.run(stream=s)
+                st.run_one_call(stream=s)
         with torch.cuda.stream(stream):
             body(stream)
         torch.cuda.synchronize()
@@ -441,7 +444,7 @@ def time_degenerate(dev, stream, flush, reps=200):
         st.check_device_errors()
         res[name] = {"ms": round(ms, 5), "tflops": round(flops / ms / 1e9, 3),
                      "kv_gbs": round(kv_bytes(wl.kv_indptr) / ms / 1e6, 2),
-                     "q_len": int(wl.q_len[0]), "num_splits": st.num_splits}
+                     "q_len": int(wl.q_len[0]), "num_splits": st.launched_splits}
     return res
 
 
@@ -461,14 +464,14 @@ def step_timeline(workload, reps=50):
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        st.run(stream=stream)
+        st.run_one_call(stream=stream)
     torch.cuda.synchronize()
     st.check_device_errors()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            st.run(stream=stream)
+            st.run_one_call(stream=stream)
 
     def replays(n):
         for _ in range(n):
@@ -502,7 +505,7 @@ def step_timeline(workload, reps=50):
     out = {name: {"start_us": round(statistics.median(a for a, _ in v), 2),
                   "end_us": round(statistics.median(b for _, b in v), 2), "steps": len(v)}
            for name, v in rows.items()}
-    return {"workload": workload, "num_splits": st.num_splits, "kernels": out}
+    return {"workload": workload, "num_splits": st.launched_splits, "kernels": out}
 
 
 def oracle_step(wl, rows=None, nthreads=0):

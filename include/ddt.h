@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define DDT_ABI_VERSION 1
+#define DDT_ABI_VERSION 2
 
 /* Sizes fixed by the absorbed-MLA layout ("The 30-Column Mask", shapes log:
  * Dl=512, Dr=64; "The Forward Pass Pseudocode": scores over c_kv and k_pe,
@@ -88,10 +88,10 @@ typedef enum {
 } ddt_status;
 
 /* Bits of the device error word (see ddt_get_error). */
-#define DDT_DEVERR_QO_INDPTR    0x001u  /* qo_indptr not matching budget+1 / q_len limits */
+#define DDT_DEVERR_QO_INDPTR    0x001u  /* qo_indptr not matching budget+1, q_len limits or [0, total_q] */
 #define DDT_DEVERR_KV_INDPTR    0x002u  /* kv_len < q_len or kv_len > max_kv_len */
 #define DDT_DEVERR_KV_INDEX     0x004u  /* a kv_indices entry outside [0, pool_rows) */
-#define DDT_DEVERR_MASK_INDPTR  0x008u  /* mask_indptr not matching q_len*ceil(kv_len/32) */
+#define DDT_DEVERR_MASK_INDPTR  0x008u  /* mask_indptr negative or not matching q_len*ceil(kv_len/32) */
 #define DDT_DEVERR_TOPK_ORDER   0x010u  /* top-k log-probs not non-increasing (or NaN) */
 #define DDT_DEVERR_EXHAUSTED    0x020u  /* budget larger than the implicit tree */
 #define DDT_DEVERR_PARENT       0x040u  /* a parent link that is not an earlier node */
@@ -184,12 +184,17 @@ ddt_status ddt_build_tree_visibility(const float *topk_logp, const int32_t *topk
 /*
  * Split-KV sizing.  ddt_verify_attn_num_splits() returns the split count the
  * library would pick for this shape on `num_sms` SMs (num_sms <= 0: query the
- * current device).  ddt_verify_attn_workspace_size() returns the workspace
- * bytes ddt_verify_attn needs for `num_splits` splits (0 bytes for one split):
- * num_splits * total_q * num_heads * (512 + 1) * 4 bytes, 256-byte aligned.
+ * current device).  A split covers ceil(max_kv_len / num_splits) kv columns
+ * rounded up to whole 64-column tiles, so fewer splits than asked may cover
+ * the range: ddt_verify_attn_launched_splits() returns how many splits a call
+ * with `num_splits` (>= 1) actually launches (1 = no combine kernel).
+ * ddt_verify_attn_workspace_size() returns the workspace bytes ddt_verify_attn
+ * needs for `num_splits` splits (0 bytes for one split): num_splits * total_q
+ * * num_heads * (512 + 1) * 4 bytes, 256-byte aligned.
  */
 int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max_q_len,
                                    int32_t max_kv_len, int32_t num_sms);
+int32_t ddt_verify_attn_launched_splits(int32_t max_kv_len, int32_t num_splits);
 size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_t num_splits);
 
 /*
@@ -208,6 +213,9 @@ size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_
  *          over the columns j in [0, kv_len_b) whose mask bit (i, j) is set,
  *   out[t,h,:] = sum_j softmax(s)_j * kv_pool[...same row..., 0:512],
  *   lse[t,h]   = log(sum_j exp(s_j))   (natural log).
+ * Every mask bit is honoured: any bit pattern is valid, not only the
+ * ancestors-plus-prefix masks of a tree.  A row with no visible column gets
+ * out = 0 and lse = -inf.
  *
  *   q           (device) bf16 [total_q][num_heads][576] (absorbed q_nope ++ roped q_pe).
  *   kv_pool     (device) bf16 [pool_rows][576] (c_kv ++ k_pe), 16-byte aligned.
@@ -215,7 +223,11 @@ size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_
  *               prefix slots followed by q_len_b tree-node slots in node order.
  *   kv_indptr   (device) int32 [batch+1]; kv_len_b = prefix_len_b + q_len_b.
  *   qo_indptr   (device) int32 [batch+1]; q_len_b <= max_q_len <= 128.
- *   mask, mask_indptr (device) as produced by ddt_compile_visibility.
+ *   mask, mask_indptr (device) bit-packed as ddt_compile_visibility writes it:
+ *               request b's rows start at word mask_indptr[b], each
+ *               ceil(kv_len_b / 32) words, bit (j mod 32) of word j / 32 is
+ *               column j.  The mask may be the output of the kernel launched
+ *               just before on the same stream.
  *   total_q     = qo_indptr[batch] (host value); max_q_len / max_kv_len are
  *               host-side upper bounds used to size the grid.
  *   num_splits  0 = choose (ddt_verify_attn_num_splits), else 1..128.
@@ -224,6 +236,12 @@ size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_
  *   workspace   (device) >= ddt_verify_attn_workspace_size(total_q, num_heads,
  *               splits) bytes, 256-byte aligned; may be NULL when one split.
  * Supported: num_heads >= 1 (up to 128).
+ * Device checks (latched, the request's rows left unwritten): q_len outside
+ * [1, max_q_len] or qo_indptr outside [0, total_q] (DDT_DEVERR_QO_INDPTR),
+ * kv_len outside [q_len, max_kv_len] or a negative kv_indptr
+ * (DDT_DEVERR_KV_INDPTR), a negative mask_indptr or a request whose words do
+ * not number q_len * ceil(kv_len / 32) (DDT_DEVERR_MASK_INDPTR), a kv_indices
+ * entry outside the pool (DDT_DEVERR_KV_INDEX: row 0 is read instead).
  */
 ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
                            const int32_t *kv_indices, const int32_t *kv_indptr,
@@ -245,7 +263,8 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
  * that loads the library holds until the process exits.
  *
  * Arguments, outputs and errors are those of ddt_verify_attn minus the
- * workspace.  With num_splits = 0 the library picks the split count as
+ * workspace.  ddt_verify_attn_noalloc_splits() returns the number of splits a
+ * call with these sizes and `num_splits` launches.  With num_splits = 0 the library picks the split count as
  * ddt_verify_attn does, but only among the counts whose split results fit
  * DDT_NOALLOC_SCRATCH_BYTES (see ddt_verify_attn_workspace_size), down to 1,
  * which needs no scratch; so a long kv range over many rows may run with
@@ -260,6 +279,8 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
  * be cleared between calls.
  */
 #define DDT_NOALLOC_SCRATCH_BYTES (32u << 20)
+int32_t ddt_verify_attn_noalloc_splits(int32_t batch, int32_t num_heads, int32_t total_q,
+                                       int32_t max_q_len, int32_t max_kv_len, int32_t num_splits);
 ddt_status ddt_verify_attn_noalloc(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
                                    const int32_t *kv_indices, const int32_t *kv_indptr,
                                    const int32_t *qo_indptr, const uint32_t *mask,
@@ -410,6 +431,11 @@ ddt_status ddt_get_error(void *stream, uint32_t *device_error);
  *
  * Each field has the meaning, layout and ownership it has in the call that
  * consumes it; `total_mask_words` = mask_indptr[batch] is the size of `mask`.
+ * The step's attention uses the mask the step has just built, a tree mask
+ * (every prefix column visible, no column after the row's own node): it reads
+ * no mask word for blocks of prefix columns, so it streams the prefix while
+ * the tree build is still running, and it skips the columns after each row
+ * tile's last node.
  * Returns the first non-OK status of the four calls; nothing after that call
  * is launched.
  */

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.ddt_abi_version() == 1
+    assert lib.ddt_abi_version() == 2
     assert lib.ddt_status_string(0) == b"ok"
     assert b"workspace" in lib.ddt_status_string(3)
 
@@ -70,6 +70,21 @@ def test_workspace_size_formula(lib):
     a = (rows * 4 * 512 * 4 + 255) // 256 * 256
     b = (rows * 4 * 4 + 255) // 256 * 256
     assert lib.ddt_verify_attn_workspace_size(33, 64, 4) == a + b
+
+
+def test_launched_splits_follow_the_tile_rounding(lib):
+    # a split covers ceil(N / s) columns rounded up to whole 64-column tiles;
+    # the splits launched are those that then cover N (no empty tail split)
+    for N in (30, 64, 65, 309, 1520, 4129, 131137):
+        for s in (1, 2, 3, 4, 7, 9, 16, 128):
+            cols = -(-N // s)
+            cols = -(-cols // 64) * 64
+            assert lib.ddt_verify_attn_launched_splits(N, s) == -(-N // cols), (N, s)
+    assert lib.ddt_verify_attn_launched_splits(1520, 7) == 6
+    assert lib.ddt_verify_attn_launched_splits(1520, 16) == 12
+    assert lib.ddt_verify_attn_launched_splits(30, 2) == 1      # one tile: nothing to split
+    assert lib.ddt_verify_attn_launched_splits(309, 2) == 2
+    assert lib.ddt_verify_attn_launched_splits(100, 0) == 1     # out of range: one split
 
 
 def test_num_splits_is_bounded(lib):

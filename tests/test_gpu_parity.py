@@ -2,9 +2,9 @@
 
 Tree, mask and accept must match bit for bit.  Attention must satisfy
 max|diff| <= 1e-2 * max|ref| and mean relative error (sum|diff| / sum|ref|)
-<= 2e-3 against the fp64 oracle (bf16 inputs, fp32 accumulation and output).
-Small workloads compare every row; the full-size ones compare sampled rows
-the oracle computes one by one, plus properties that hold at any size.
+<= 2e-3 against the fp64 oracle (bf16 inputs, fp32 accumulation and output),
+over every row of every workload, the five full-size ones included; a few
+extra cases at full size compare sampled rows the oracle computes one by one.
 """
 import numpy as np
 import pytest
@@ -95,25 +95,30 @@ def test_tiny_shapes_log_workload():
     _full_check(workloads.preset("tiny_p21_b8_h8"), n_rows=10 ** 9)
 
 
+ALL = 10 ** 9   # every row
+
+
 def test_single_request_full_heads():
-    _full_check(workloads.preset("single_p4096_b32_h64"), n_rows=512)
+    st, _ = _full_check(workloads.preset("single_p4096_b32_h64"), n_rows=ALL)
+    assert st.launched_splits > 1   # the timed shape splits: the combine is covered
 
 
 def test_ragged_batch():
-    _full_check(workloads.preset("ragged_bs8_b32_h64"), n_rows=160)
+    _full_check(workloads.preset("ragged_bs8_b32_h64"), n_rows=ALL)
 
 
 def test_long_context_split_kv():
+    # every one of the 4160 rows, with 1% of kv rows scaled by 8 (rescales)
     wl = workloads.preset("long_p131072_b64_h64")
-    st, _ = _full_check(wl, n_rows=48)
-    assert st.num_splits > 1
+    st, _ = _full_check(wl, n_rows=ALL)
+    assert st.launched_splits > 1
 
 
 def test_mixed_budgets_with_half_matching_targets():
     wl = workloads.preset("mixed_bs32_b16or32_h16")
     tok, par, _ = _oracle_tree(wl)
     argmax = oracle.best_child_argmax(par, wl.qo_indptr, tok, wl.argmax_coin, wl.argmax_random)
-    st, _ = _full_check(wl, n_rows=256, argmax=argmax)
+    st, _ = _full_check(wl, n_rows=ALL, argmax=argmax)
     assert st.accept_len.max().item() > 1   # the 50% matches do get accepted
 
 
@@ -126,10 +131,14 @@ def test_chain_forcing_targets_accept_deep_paths():
     assert st.accept_len.item() >= 2
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
-def test_forced_split_counts_agree(splits):
+# requested -> launched: a split covers ceil(1506 / s) columns rounded up to
+# whole 64-column tiles, and only the splits that then cover the 1506 columns
+# of the longest request run
+@pytest.mark.parametrize("splits,launched", [(1, 1), (2, 2), (3, 3), (7, 6), (16, 12), (24, 24)])
+def test_forced_split_counts_agree(splits, launched):
     wl = workloads.make_workload("splits", 99, 2, 16, [700, 1500], [20, 5], 4, 1000, 2.0)
-    _full_check(wl, n_rows=10 ** 9, num_splits=splits)
+    st, _ = _full_check(wl, n_rows=10 ** 9, num_splits=splits)
+    assert int(wl.kv_len.max()) == 1506 and st.launched_splits == launched
 
 
 @pytest.mark.parametrize("H", [1, 3, 16, 17, 128])
@@ -429,6 +438,91 @@ def test_wrong_mask_stride_is_rejected():
     torch.cuda.synchronize()
     status, bits = ddt.ddt_get_error()
     assert status == 5 and bits & 0x8
+
+
+def _custom_mask_case(splits):
+    """A visibility mask that is not a tree mask: every bit counts."""
+    wl = workloads.make_workload("custom_mask", 909, 2, 8, [130, 61], [12, 20], 4, 3000, 2.0)
+    st = _step(wl, num_splits=splits)
+    tok, par, _ = _oracle_tree(wl)
+    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    mask = mask.copy()
+
+    def flip(b, i, c, on):
+        W = (int(wl.kv_len[b]) + 31) // 32
+        w = int(mip[b]) + i * W + c // 32
+        if on:
+            mask[w] |= np.uint32(1 << (c % 32))
+        else:
+            mask[w] &= np.uint32(~(1 << (c % 32)) & 0xFFFFFFFF)
+
+    P0, P1 = int(wl.prefix_len[0]), int(wl.prefix_len[1])
+    flip(0, 3, 5, False)          # a hidden prefix column
+    for c in range(64, 128):      # a whole 64-column block of prefix hidden for node 4
+        flip(0, 4, c, False)
+    flip(0, 1, P0 + 7, True)      # a column after the row's own node made visible
+    flip(1, 2, P1 + 19, True)     # the last tree column seen from an early node
+    flip(1, 0, 0, False)          # the root of request 1 loses prefix column 0
+    W1 = (int(wl.kv_len[1]) + 31) // 32
+    row = int(mip[1]) + 5 * W1    # node 5 of request 1 sees nothing at all
+    mask[row:row + W1] = 0
+    return wl, st, mask, mip
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_verify_attn_honours_every_mask_bit(splits):
+    # ddt_verify_attn takes any bit pattern: hidden prefix columns (one alone,
+    # a whole block), visible columns after a row's own node, and a row that
+    # sees nothing (out 0, lse -inf) all match the oracle, which honours every bit
+    from tree_speculative_decoding_gb300 import ddt
+    wl, st, mask, mip = _custom_mask_case(splits)
+    dmask = torch.from_numpy(mask.view(np.int32)).to("cuda:0")
+    out = torch.full_like(st.out, float("nan"))
+    lse = torch.full_like(st.lse, float("nan"))
+    ddt.ddt_verify_attn(st.q, st.kv_pool, st.kv_indices, st.kv_indptr, st.qo_indptr, dmask,
+                        st.mask_indptr, wl.scale, out, lse, max_q_len=st.max_q_len,
+                        max_kv_len=st.max_kv_len, num_splits=splits, workspace=st.workspace)
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (0, 0)
+    ref, ref_lse = oracle.verify_attn(wl.q, wl.kv_pool, wl.kv_indices, wl.kv_indptr,
+                                      wl.qo_indptr, mask, mip, wl.H, wl.scale)
+    got = out.reshape(-1, 512).double().cpu().numpy()
+    got_lse = lse.reshape(-1).double().cpu().numpy()
+    empty = np.isneginf(ref_lse)
+    assert empty.sum() == wl.H                     # node 5 of request 1, every head
+    assert np.array_equal(np.isneginf(got_lse), empty) and (got[empty] == 0).all()
+    diff = np.abs(got - ref)
+    assert diff.max() <= MAX_TOL * np.abs(ref).max()
+    assert diff.sum() / np.abs(ref).sum() <= MEAN_TOL
+    np.testing.assert_allclose(got_lse[~empty], ref_lse[~empty], rtol=1e-4, atol=1e-3)
+    # the same step's own tree mask gives different rows where bits were flipped
+    assert not np.allclose(got, st.out.reshape(-1, 512).double().cpu().numpy())
+
+
+def test_inconsistent_offsets_are_latched_and_nothing_is_written():
+    # qo_indptr past total_q, a negative qo_indptr and a negative mask_indptr,
+    # each made on the host: the attention latches the bit and writes no row
+    from tree_speculative_decoding_gb300 import ddt
+    wl = workloads.make_workload("offsets", 31, 2, 8, [40, 70], [6, 9], 4, 500, 2.0)
+    st = _step(wl, num_splits=1)
+    cases = [("qo", torch.tensor([0, 7, st.total_q + 9], dtype=torch.int32), 0x1),
+             ("qo", torch.tensor([-3, 7, st.total_q], dtype=torch.int32), 0x1),
+             ("mask", torch.tensor([-1, st.mask_indptr_host[1].item(), st.mask_indptr_host[2].item()],
+                                   dtype=torch.int32), 0x8)]
+    for which, bad, bit in cases:
+        qo = bad.to("cuda:0") if which == "qo" else st.qo_indptr
+        mip = bad.to("cuda:0") if which == "mask" else st.mask_indptr
+        out = torch.full_like(st.out, 7.0)
+        ddt.ddt_verify_attn(st.q, st.kv_pool, st.kv_indices, st.kv_indptr, qo, st.mask, mip,
+                            wl.scale, out, None, max_q_len=st.max_q_len, max_kv_len=st.max_kv_len,
+                            num_splits=1)
+        torch.cuda.synchronize()
+        status, bits = ddt.ddt_get_error()
+        assert status == 5 and bits & bit, (which, hex(bits))
+        # request 0's rows: untouched when its own offsets are the bad ones
+        if which == "mask" or bad[0] < 0:
+            assert bool((out[:7] == 7.0).all())
+    assert ddt.ddt_get_error() == (0, 0)
 
 
 def test_bad_budget_indptr_is_latched():

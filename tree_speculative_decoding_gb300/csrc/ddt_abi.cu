@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -18,7 +19,9 @@ __device__ unsigned int g_ddt_error_word;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-    bool ready = false;
+    // set (release) after err and num_sms are written; read (acquire) before
+    // they are used, so a thread that sees it set also sees them
+    std::atomic<bool> ready{false};
     unsigned int *err = nullptr;  // device address of g_ddt_error_word
     int num_sms = 0;
 };
@@ -33,9 +36,9 @@ DeviceState *device_state() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     DeviceState &st = g_dev[dev];
-    if (st.ready) return &st;
+    if (st.ready.load(std::memory_order_acquire)) return &st;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!st.ready) {
+    if (!st.ready.load(std::memory_order_relaxed)) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_ddt_error_word) != cudaSuccess) return nullptr;
         int sms = 0;
@@ -44,7 +47,7 @@ DeviceState *device_state() {
         if (ddt::attn_prepare_device() != cudaSuccess) return nullptr;
         st.err = static_cast<unsigned int *>(p);
         st.num_sms = sms;
-        st.ready = true;
+        st.ready.store(true, std::memory_order_release);
     }
     return &st;
 }
@@ -158,6 +161,11 @@ int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max
     return choose_splits(batch, num_heads, max_q_len, max_kv_len, num_sms);
 }
 
+int32_t ddt_verify_attn_launched_splits(int32_t max_kv_len, int32_t num_splits) {
+    if (max_kv_len < 1 || num_splits < 1) return 1;
+    return ddt::attn_launched_splits(max_kv_len, num_splits);
+}
+
 size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_t num_splits) {
     if (total_q < 1 || num_heads < 1 || num_splits <= 1) return 0;
     const size_t rows = (size_t)total_q * num_heads;
@@ -165,13 +173,19 @@ size_t ddt_verify_attn_workspace_size(int32_t total_q, int32_t num_heads, int32_
            align256(rows * num_splits * sizeof(float));
 }
 
-ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
-                           const int32_t *kv_indices, const int32_t *kv_indptr,
-                           const int32_t *qo_indptr, const uint32_t *mask,
-                           const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
-                           int32_t total_q, int32_t max_q_len, int32_t max_kv_len, float scale,
-                           int32_t num_splits, float *out, float *lse, void *workspace,
-                           size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+// ddt_verify_attn with the mask's provenance: tree_mask = 1 only where the
+// mask was built by this library's tree + visibility kernel earlier in the
+// same step (ddt_verify_step), so that its prefix columns are known visible.
+ddt_status verify_attn_impl(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
+                            const int32_t *kv_indices, const int32_t *kv_indptr,
+                            const int32_t *qo_indptr, const uint32_t *mask,
+                            const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
+                            int32_t total_q, int32_t max_q_len, int32_t max_kv_len, float scale,
+                            int32_t num_splits, float *out, float *lse, void *workspace,
+                            size_t workspace_bytes, void *stream, int tree_mask) {
     if (!q || !kv_pool || !kv_indices || !kv_indptr || !qo_indptr || !mask || !mask_indptr ||
         !out)
         return DDT_ERR_INVALID_ARG;
@@ -186,13 +200,11 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
     DeviceState *st = device_state();
     if (!st) return DDT_ERR_CUDA;
 
-    int splits = num_splits > 0
+    const int requested = num_splits > 0
         ? num_splits
         : choose_splits(batch, num_heads, max_q_len, max_kv_len, st->num_sms);
-    const int tile = ddt::attn_kv_tile();
-    int split_cols = (max_kv_len + splits - 1) / splits;
-    split_cols = (split_cols + tile - 1) / tile * tile;
-    splits = (max_kv_len + split_cols - 1) / split_cols;  // no empty tail splits
+    int split_cols = 0, splits = 1;
+    ddt::attn_split_layout(max_kv_len, requested, &split_cols, &splits);
 
     ddt::AttnArgs a;
     memset(&a, 0, sizeof a);
@@ -212,6 +224,7 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
     a.scale = scale;
     a.num_splits = splits;
     a.split_cols = split_cols;
+    a.tree_mask = tree_mask;
     a.out = out;
     a.lse = lse;
     a.err = st->err;
@@ -228,6 +241,21 @@ ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t p
     cudaError_t e = ddt::launch_attn_partial(a, s);
     if (e == cudaSuccess && splits > 1) e = ddt::launch_attn_combine(a, s);
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+ddt_status ddt_verify_attn(const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows,
+                           const int32_t *kv_indices, const int32_t *kv_indptr,
+                           const int32_t *qo_indptr, const uint32_t *mask,
+                           const int32_t *mask_indptr, int32_t batch, int32_t num_heads,
+                           int32_t total_q, int32_t max_q_len, int32_t max_kv_len, float scale,
+                           int32_t num_splits, float *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    return verify_attn_impl(q, kv_pool, pool_rows, kv_indices, kv_indptr, qo_indptr, mask,
+                            mask_indptr, batch, num_heads, total_q, max_q_len, max_kv_len, scale,
+                            num_splits, out, lse, workspace, workspace_bytes, stream, 0);
 }
 
 ddt_status ddt_accept(const int32_t *node_token, const int32_t *parent,
@@ -331,10 +359,11 @@ ddt_status ddt_verify_step(const ddt_step_args *a, void *stream) {
                                               a->batch, a->max_depth, a->topk, a->node_token,
                                               a->parent, a->depth, a->mask, stream);
     if (st != DDT_OK) return st;
-    st = ddt_verify_attn(a->q, a->kv_pool, a->pool_rows, a->kv_indices, a->kv_indptr,
-                         a->qo_indptr, a->mask, a->mask_indptr, a->batch, a->num_heads,
-                         a->total_q, a->max_q_len, a->max_kv_len, a->scale, a->num_splits,
-                         a->out, a->lse, a->workspace, a->workspace_bytes, stream);
+    // the mask was just built by ddt_build_tree_visibility: a tree mask
+    st = verify_attn_impl(a->q, a->kv_pool, a->pool_rows, a->kv_indices, a->kv_indptr,
+                          a->qo_indptr, a->mask, a->mask_indptr, a->batch, a->num_heads,
+                          a->total_q, a->max_q_len, a->max_kv_len, a->scale, a->num_splits,
+                          a->out, a->lse, a->workspace, a->workspace_bytes, stream, 1);
     if (st != DDT_OK) return st;
     st = ddt_accept(a->node_token, a->parent, a->qo_indptr, a->target_argmax, a->batch,
                     a->max_depth, a->accept_len, a->accepted_nodes, a->commit_tokens, a->bonus,

@@ -44,9 +44,22 @@
 //   * Warp roles: warps 0-3 softmax / epilogue (thread = row = TMEM lane);
 //     of warps 4-6, one issues the MMAs (placed next to a non-owner softmax
 //     warp) and two are producers.
+//   * Q: the tile's rows are one contiguous block of q, so the MMA warp loads
+//     this CTA's half with TMA tensor tiles as soon as the request's offsets
+//     are known: the rope box lands in its 64-byte-swizzled operand layout,
+//     the latent boxes are staged in the second half of the stage ring and
+//     moved into tensor memory with tcgen05.cp.
+//   * The visibility mask: by default every mask bit is honoured (a block
+//     whose bits are all ones skips the per-column test; each block's words
+//     are loaded one block ahead).  When the caller states that the mask is a
+//     tree mask built by this library in the same step (every prefix column
+//     visible, no column after the row's own node), prefix-only blocks read no
+//     mask word, so the attention streams the prefix while the tree build is
+//     still running, and columns after the tile's last node are skipped.
 //   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
 //     stops, and still meets its partner at the final cluster barrier.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -84,7 +97,7 @@ constexpr int kOffBar = kOffLinv + 64 * 4;
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL0 = B_EMPTY0 + kStages, B_SFULL1, B_SFREE0, B_SFREE1,
     B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
-    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_ODONE, B_COUNT
+    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_ODONE, B_QLD, B_QFREE, B_COUNT
 };
 constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // 2 buffers x 2 owner warps: 4-byte "read" signals
 constexpr int kOffHolder = kOffXsig + 16;
@@ -119,9 +132,19 @@ static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 
 static_assert(kRows * kORowStride <= kStages * kStageBytes, "epilogue staging fits in the stages");
 
 struct TcParams {
+    // q viewed as [total_q * num_heads rows][576] bf16: boxes of 128 rows x 64
+    // latent dims (128-byte swizzle) and 128 rows x 32 rope dims (64-byte swizzle)
+    CUtensorMap q_lat;
+    CUtensorMap q_rope;
     AttnArgs a;
     int tiles_per_req;
 };
+// The tile's Q latent half is staged by TMA in stages 2 and 3 (4 boxes of 16
+// KB), copied into tensor memory by tcgen05.cp, and the two stages are then
+// handed to the producers.
+constexpr int kOffQStage = kOffStage + 2 * kStageBytes;
+constexpr uint32_t kQBytes = 4 * kRows * 128 + kRows * 64;
+static_assert(4 * kRows * 128 <= 2 * kStageBytes, "Q staging fits in two stages");
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
                                               unsigned int *err) {
@@ -130,6 +153,23 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     *abort = 1;
     latch(err, DDT_DEVERR_TIMEOUT);
     return false;
+}
+// The same wait for a whole warp: it succeeds for every lane or for none, so
+// the warp stays converged for the warp-collective instructions after it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned int *err) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort, err));
+}
+
+__device__ __forceinline__ float max64(const float (&v)[kNb]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(fmaxf(v[4 * i], v[4 * i + 1]), fmaxf(v[4 * i + 2], v[4 * i + 3]));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -153,8 +193,28 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     pdl_trigger();
     const uint32_t rank = cluster_ctarank();  // 0 or 1: latent half
     const uint32_t peer = rank ^ 1u;
-    const int split = blockIdx.x >> 1;
-    const int tile = blockIdx.y;
+    // Clusters run tile-fastest: the row tiles that share a split's kv columns
+    // are dispatched together, so that one wave reads those rows from HBM once.
+    const int tile = blockIdx.x >> 1;
+    const int split = blockIdx.y;
+    const int mma_warp = rank ? 4 : 6;
+    // The MMA warp's first lane sets up the barriers at once, so that it can
+    // start the Q copies as soon as the request's offsets are known; the other
+    // threads use the barriers only after the set-up's block barrier.
+    if (warp == mma_warp && lane == 0) {
+        for (int i = 0; i < B_COUNT; ++i) {
+            // one arrival: stage empties, score full, PV done, O done, Q (MMA
+            // commits or a TMA)
+            uint32_t count = 1;
+            if (i < B_EMPTY0) count = 64;                       // stage full: 64 producer lanes
+            else if (i == B_SFREE0 || i == B_SFREE1 || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
+            else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
+            else if (i == B_FIN) count = 2;
+            mbar_init(bar(i), count);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
     // Clusters are dispatched in block-index order, request by request.  With
     // several requests, blockIdx.z = k takes the request with the k-th most kv
     // columns (ties by index), so the longest requests start first and a long
@@ -177,27 +237,37 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     }
 
     // ---- work of this tile / split (identical in both CTAs of the pair) ----
+    // All six offsets of the request are loaded in one round of independent
+    // loads: after an L2 flush each dependent round trip costs ~1.6 us.
     const int H = a.num_heads;
-    const int qo0 = a.qo_indptr[b];
-    const int T = a.qo_indptr[b + 1] - qo0;
-    const int kv0 = a.kv_indptr[b];
-    const int N = a.kv_indptr[b + 1] - kv0;
+    const int qo0 = a.qo_indptr[b], qo1 = a.qo_indptr[b + 1];
+    const int kv0 = a.kv_indptr[b], kv1 = a.kv_indptr[b + 1];
+    const int m0 = a.mask_indptr[b], m1 = a.mask_indptr[b + 1];
+    const int T = qo1 - qo0;
+    const int N = kv1 - kv0;
+    const int W = (N + 31) >> 5;
+    // rows of q and out: [qo0, qo1) within [0, total_q); kv columns [kv0, kv1);
+    // mask words [m0, m1) as q_len rows of ceil(kv_len / 32) words
+    const bool bad_qo = T < 1 || T > a.max_q_len || qo0 < 0 || qo1 > a.total_q;
+    const bool bad_kv = N < T || N > a.max_kv_len || kv0 < 0;
+    const bool bad_mask = !bad_qo && !bad_kv && (m0 < 0 || m1 - m0 != T * W);
+    if (bad_qo || bad_kv || bad_mask) {  // uniform in the pair: no cluster interaction yet
+        if (tid == 0 && rank == 0)
+            latch(a.err, (bad_qo ? DDT_DEVERR_QO_INDPTR : 0u) | (bad_kv ? DDT_DEVERR_KV_INDPTR : 0u) |
+                             (bad_mask ? DDT_DEVERR_MASK_INDPTR : 0u));
+        pdl_wait();
+        return;
+    }
     const int rows_req = T * H;
     const int row0 = tile * kRows;
-    if (row0 >= rows_req) { pdl_wait(); return; }  // uniform in the pair: no cluster interaction yet
-    bool bad = false;
-    if (T > a.max_q_len || T < 1) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_QO_INDPTR); }
-    if (N < T || N > a.max_kv_len) { bad = true; if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_KV_INDPTR); }
+    if (row0 >= rows_req) { pdl_wait(); return; }  // uniform in the pair
     const int P = N - T;
-    const int W = (N + 31) >> 5;
-    if (!bad && a.mask_indptr[b + 1] - a.mask_indptr[b] != T * W) {
-        bad = true;
-        if (tid == 0 && rank == 0) latch(a.err, DDT_DEVERR_MASK_INDPTR);
-    }
-    if (bad) { pdl_wait(); return; }  // uniform in the pair
     const int rows_valid = min(kRows, rows_req - row0);
     const int i_max = (row0 + rows_valid - 1) / H;   // last node in the tile
-    const int kv_end = P + i_max + 1;                 // nothing beyond is visible to the tile
+    // A library-built tree mask shows no column after the row's own node, so
+    // nothing beyond P + i_max is visible to the tile; any other mask may set
+    // any bit of the row.
+    const int kv_end = a.tree_mask ? P + i_max + 1 : N;
     const int c_begin = split * a.split_cols;
     const int c_end = min(kv_end, c_begin + a.split_cols);
     const int nblk = (c_end > c_begin) ? (c_end - c_begin + kNb - 1) / kNb : 0;
@@ -218,11 +288,17 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         return;
     }
 
-    // ---- loads that need no set-up, issued before it so that the barrier
-    // init, the tensor-memory allocation and the cluster sync run under their
-    // latency: the softmax warps' Q row, the producers' first kStages blocks of
-    // kv slots ----
-    const int mma_warp = rank ? 4 : 6;
+    // ---- loads that need no set-up, issued before it so that the tensor-memory
+    // allocation and the cluster sync run under their latency: the tile's Q
+    // (TMA, by the MMA warp) and the producers' first kStages blocks of kv slots ----
+    if (warp == mma_warp && lane == 0) {
+        const int y = (qo0 * H) + row0;  // first (node, head) row of the tile in q
+        mbar_arrive_expect_tx(bar(B_QLD), kQBytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            tma_load_2d(sbase + kOffQStage + k * kRows * 128, &prm.q_lat, 256 * (int)rank + 64 * k, y, bar(B_QLD));
+        tma_load_2d(sbase + kOffQr, &prm.q_rope, 512 + 32 * (int)rank, y, bar(B_QLD));
+    }
     const bool producer = warp >= 4 && warp != mma_warp;
     const int half = (warp == (rank ? 5 : 4)) ? 0 : 1;  // producers: kv rows [32 half, 32 half + 32)
     // slot of this producer lane's kv row of block j
@@ -235,35 +311,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         for (int s = 0; s < kStages; ++s) slot_ahead[s] = (s < nblk) ? fetch_slot(s) : 0;
     }
     const int r = tid;  // row within the tile for warps 0-3
-    uint4 xl[32], xr[4];
-    if (warp < 4) {
-        const bool valid = r < rows_valid;
-        const int rr = row0 + r;
-        const uint4 *src = nullptr;
-        if (valid) {
-            const int64_t grow = (int64_t)(qo0 + rr / H) * H + (rr % H);
-            src = reinterpret_cast<const uint4 *>(a.q + grow * DDT_D);
-        }
-#pragma unroll
-        for (int v = 0; v < 32; ++v) xl[v] = valid ? src[(256 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) xr[v] = valid ? src[(512 + 32 * rank) / 8 + v] : make_uint4(0, 0, 0, 0);
-    }
 
     // ---- setup ----
-    if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i) {
-            uint32_t count = 1;  // stage empties, score full, PV done: one MMA commit
-            if (i < B_EMPTY0) count = 64;                       // stage full: 64 producer lanes
-            else if (i == B_SFREE0 || i == B_SFREE1 || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
-            else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
-            else if (i == B_FIN) count = 2;
-            // B_ODONE: the single commit after the last PV
-            mbar_init(bar(i), count);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
     if (warp == 5) tmem_alloc(smem_u32(holder), kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -283,27 +332,30 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         for (int q = 0; q < kNb / 32; ++q) tmem_st32(tmem + lane_off + kColS + kNb * sb + 32 * q, z);
         tmem_wait_st();
     };
-    if (warp < 4) {  // this CTA's half of Q into tensor memory (thread = row = lane)
-        uint32_t w[32];
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {  // latent: 4 x 64 dims
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const uint4 x = xl[8 * part + v];
-                w[4 * v + 0] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + kColQ + 32 * part, w);
-        }
-#pragma unroll
-        for (int v = 0; v < 4; ++v)  // rope half: 32 dims as a 64-byte-swizzled K-major row
-            *reinterpret_cast<uint4 *>(smem + kOffQr + (r >> 3) * 512 + (r & 7) * 64 +
-                                       ((v ^ ((r >> 1) & 3)) << 4)) = xr[v];
-        fence_proxy_async_smem();  // read by the tensor core
+    if (warp < 4) {  // O and both score blocks start at zero
         const uint32_t z[32] = {};
 #pragma unroll
         for (int q = 0; q < 8; ++q) tmem_st32(tmem + lane_off + kColO + 32 * q, z);
         zero_scores(0);
         zero_scores(1);
+    }
+    // Q's latent half from the staging boxes into tensor memory (columns kColQ +
+    // 8 ks hold dims [16 ks, 16 ks + 16) as bf16 pairs, the layout of an MMA A
+    // operand); the commit hands stages 2 and 3 to the producers.
+    bool q_in = true;
+    if (warp == mma_warp) {
+        if (lane == 0) {
+            q_in = wait_or_abort(bar(B_QLD), 0, abort_flag, a.err);
+            if (q_in) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks)
+                    tmem_cp_128x256b(tmem + kColQ + 8 * ks,
+                                     smem_desc(sbase + kOffQStage + (ks >> 2) * kRows * 128 + (ks & 3) * 32, 16, 1024));
+                mma_commit(bar(B_QFREE));
+            }
+        }
+        __syncwarp();
     }
     // Q / O / S in tensor memory before the first MMA: the softmax warps and the
     // MMA warp meet on a named barrier; the producers start gathering at once.
@@ -335,8 +387,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             for (int s = 0; s < kStages; ++s) {
                 const int j = j0 + s, u = j0 / kStages;
                 if (j >= nblk) break;
-                if (*abort_flag) { run = false; break; }
-                if (u >= 1 && !wait_or_abort(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) { run = false; break; }
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) { run = false; break; }
+                if (u >= 1 && !warp_wait(bar(B_EMPTY0 + s), (u - 1) & 1, abort_flag, a.err)) { run = false; break; }
+                // stages 2 and 3 hold the staged Q until it is in tensor memory
+                if (u == 0 && s == 2 && !warp_wait(bar(B_QFREE), 0, abort_flag, a.err)) { run = false; break; }
                 const uint32_t stage = sbase + kOffStage + s * kStageBytes;
                 int mine = slot_ahead[s];
                 if (mine < 0 || (int64_t)mine >= a.pool_rows) {
@@ -432,7 +486,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         const int rr = row0 + r;
         const int node = row_valid ? rr / H : 0;
         const int head = row_valid ? rr % H : 0;
-        const uint32_t *mrow = a.mask + a.mask_indptr[b] + (int64_t)node * W;
+        const uint32_t *mrow = a.mask + m0 + (int64_t)node * W;
         const float sc = a.scale * kLog2e;
         // cluster addresses of the partner's buffers / barriers
         const uint32_t peer_base = map_to_cta(sbase, peer);
@@ -440,7 +494,28 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        // Visibility words.  Prefix-only blocks of a library-built tree mask read
+        // none.  The mask may be the previous kernel's output: it is waited for
+        // once, before the first word is read.  A block's two words (64 columns
+        // from c0, a multiple of 64) are loaded one block ahead, so that their
+        // latency hides behind the previous block.
+        auto all_prefix = [&](int j) {
+            const int c0 = c_begin + j * kNb;
+            return a.tree_mask && c0 + kNb <= min(P, c_end);
+        };
         bool mask_ready = false;
+        int nj = -1;  // the block whose words nw0 / nw1 hold
+        uint32_t nw0 = 0, nw1 = 0;
+        auto fetch_bits = [&](int j) {
+            if (!mask_ready) {
+                pdl_wait();
+                mask_ready = true;
+            }
+            const int w0 = (c_begin + j * kNb) >> 5;
+            nw0 = (w0 < W) ? mrow[w0] : 0u;
+            nw1 = (w0 + 1 < W) ? mrow[w0 + 1] : 0u;
+            nj = j;
+        };
 
         // read S_j into registers, clear it, and hand the score buffer back to the MMA warp
         auto take_scores = [&](int j, float (&sv)[kNb]) {
@@ -542,6 +617,15 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 float sv[kNb];
                 if (!wait_or_abort(bar(B_SFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
                 take_scores(j, sv);
+                const int c0 = c_begin + j * kNb;
+                const bool pre_only = all_prefix(j);
+                uint32_t mw0 = 0xffffffffu, mw1 = 0xffffffffu;
+                if (!pre_only) {
+                    if (nj != j) fetch_bits(j);
+                    mw0 = nw0;
+                    mw1 = nw1;
+                }
+                if (j + 1 < nblk && !all_prefix(j + 1)) fetch_bits(j + 1);
                 // owner: partner partial + own partial -> softmax -> P for both CTAs
                 if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + s), 32 * kNb * 4);
                 if (!wait_or_abort(bar(B_XFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
@@ -559,43 +643,27 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 if (lane == 0)
                     st_async_b32(map_to_cta(sbase + kOffXsig + 4 * (2 * s + (warp & 1)), peer), 0u,
                                  map_to_cta(bar(B_XEMPTY0 + s), peer));
-                // mask: prefix columns are visible to every row; only blocks reaching
-                // the tree columns (at most two per split) read mask words.  Rows past
-                // the tile's last valid row carry Q = 0 (finite scores) and are never
-                // stored, so they follow whichever path their block takes.
-                const int c0 = c_begin + j * kNb;
-                float mb = -INFINITY;
-                if (c0 + kNb <= min(P, c_end)) {
-#pragma unroll
-                    for (int k = 0; k < kNb; ++k) mb = fmaxf(mb, sv[k]);
-                } else {
-                    if (!mask_ready) {  // the mask is the visibility compile's output
-                        pdl_wait();
-                        mask_ready = true;
-                    }
-                    // 64-bit visibility window of this row starting at column c0:
-                    // mask bits, or-ed with the prefix, and-ed with the split's range
-                    const int w0 = c0 >> 5, sh = c0 & 31;
-                    uint32_t mw[3];
-#pragma unroll
-                    for (int t = 0; t < 3; ++t) mw[t] = (w0 + t < W) ? mrow[w0 + t] : 0u;
-                    const int npre = max(0, min(kNb, P - c0));       // leading prefix columns
-                    const int nin = max(0, min(kNb, c_end - c0));    // columns inside the split
+                // visibility of the block's 64 columns: the mask bits (for a tree mask,
+                // or-ed with the prefix), and-ed with the split's range.  Rows past
+                // the tile's last valid row are never stored; their scores are finite
+                // (q rows of the next request, or zeros past the end of q).
+                if (!pre_only) {
+                    const int npre = a.tree_mask ? max(0, min(kNb, P - c0)) : 0;  // leading prefix columns
+                    const int nin = max(0, min(kNb, c_end - c0));                 // columns inside the split
                     uint32_t vbits[2];
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
-                        const uint32_t v = __funnelshift_r(mw[t], mw[t + 1], sh);
                         const int lo = 32 * t;
                         const uint32_t pre = npre >= lo + 32 ? 0xffffffffu : (npre > lo ? (1u << (npre - lo)) - 1u : 0u);
                         const uint32_t in = nin >= lo + 32 ? 0xffffffffu : (nin > lo ? (1u << (nin - lo)) - 1u : 0u);
-                        vbits[t] = (v | pre) & in;
+                        vbits[t] = ((t ? mw1 : mw0) | pre) & in;
                     }
+                    if ((vbits[0] & vbits[1]) != 0xffffffffu) {
 #pragma unroll
-                    for (int k = 0; k < kNb; ++k) {
-                        sv[k] = ((vbits[k >> 5] >> (k & 31)) & 1u) ? sv[k] : -INFINITY;
-                        mb = fmaxf(mb, sv[k]);
+                        for (int k = 0; k < kNb; ++k) sv[k] = ((vbits[k >> 5] >> (k & 31)) & 1u) ? sv[k] : -INFINITY;
                     }
                 }
+                float mb = max64(sv);
                 mb *= sc;  // scores in log2 units: s * scale * log2(e)
                 float alpha = 1.0f;
                 if (mb > m_ref + kRescaleLog2) {  // also true for the first visible block (m_ref = -inf)
@@ -702,6 +770,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     }
 
     // ---- teardown: nobody leaves while the partner may still write here ----
+    if (warp == mma_warp && lane == 0 && !q_in) mbar_wait(bar(B_QLD), 0, kWaitLimit);  // Q copies in flight
     pdl_wait();  // every path waits once, so this grid ends after the previous one
     tc_fence_before();
     __syncthreads();
@@ -738,6 +807,20 @@ cudaError_t attn_tc_prepare_device() {
 }
 
 int attn_kv_tile() { return kNb; }
+
+void attn_split_layout(int max_kv_len, int requested, int *split_cols, int *splits) {
+    const int want = requested < 1 ? 1 : requested;
+    int cols = (max_kv_len + want - 1) / want;
+    cols = (cols + kNb - 1) / kNb * kNb;
+    *split_cols = cols;
+    *splits = (max_kv_len + cols - 1) / cols;
+}
+
+int attn_launched_splits(int max_kv_len, int requested) {
+    int cols = 0, splits = 1;
+    attn_split_layout(max_kv_len, requested, &cols, &splits);
+    return splits;
+}
 
 cudaError_t attn_prepare_device() {
     cudaError_t e = attn_combine_prepare_device();
@@ -782,11 +865,45 @@ int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, 
     return (int)best;
 }
 
+namespace {
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// q as a [rows][576] bf16 tensor with boxes of kRows rows x box_cols columns
+bool encode_q_map(CUtensorMap *map, const uint16_t *q, int64_t rows, uint32_t box_cols,
+                  CUtensorMapSwizzle swizzle) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)DDT_D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)DDT_D * 2};
+    const cuuint32_t box[2] = {box_cols, (cuuint32_t)kRows};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(q), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_attn_partial(const AttnArgs &a, cudaStream_t s) {
     TcParams prm;
+    const int64_t rows = (int64_t)a.total_q * a.num_heads;
+    if (!encode_q_map(&prm.q_lat, a.q, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_q_map(&prm.q_rope, a.q, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     prm.a = a;
     prm.tiles_per_req = (a.max_q_len * a.num_heads + kRows - 1) / kRows;
-    dim3 grid(2 * a.num_splits, prm.tiles_per_req, a.batch);
+    dim3 grid(2 * prm.tiles_per_req, a.num_splits, a.batch);
     return launch_pdl(attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, prm);
 }
 

@@ -104,6 +104,10 @@ struct AttnArgs {
     float scale;
     int num_splits;
     int split_cols;       // kv columns per split (multiple of the kv tile)
+    // 1 when the mask is a tree mask this library built in the same step (every
+    // prefix column visible, no column after the row's own node): prefix-only
+    // blocks then read no mask word.  0: every mask bit is honoured.
+    int tree_mask;
     float *out;           // [total_q, H, 512]
     float *lse;           // [total_q, H] or null
     float *o_part;        // [splits, total_q*H, 512] when num_splits > 1
@@ -131,6 +135,11 @@ cudaError_t launch_wait_timeout_selftest(uint32_t poll_limit, unsigned int *err,
 
 // kv columns per split must be a multiple of this (the attention kv tile)
 int attn_kv_tile();
+// The split layout a requested count (>= 1) gives: kv columns per split,
+// rounded up to whole kv tiles, and the number of splits that then cover
+// max_kv_len (no empty tail split), which can be fewer than requested.
+void attn_split_layout(int max_kv_len, int requested, int *split_cols, int *splits);
+int attn_launched_splits(int max_kv_len, int requested);
 
 // Once per device, with that device current and before any stream capture:
 // kernel attributes (dynamic shared memory opt-in).

@@ -47,7 +47,28 @@ void *scratch_address() {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The split count asked of the kernels: num_splits as given, or for 0 the
+// library's choice among the counts whose partials fit the scratch.
+int noalloc_requested_splits(int32_t batch, int32_t num_heads, int32_t total_q, int32_t max_q_len,
+                             int32_t max_kv_len, int32_t num_splits) {
+    if (num_splits > 0) return num_splits;
+    int cap = DDT_MAX_SPLITS;
+    while (cap > 1 &&
+           ddt_verify_attn_workspace_size(total_q, num_heads, cap) > (size_t)DDT_NOALLOC_SCRATCH_BYTES)
+        --cap;
+    return ddt::attn_choose_splits(batch, num_heads, max_q_len, max_kv_len, ddt::device_sm_count(), cap);
+}
+
 }  // namespace
+
+extern "C" int32_t ddt_verify_attn_noalloc_splits(int32_t batch, int32_t num_heads, int32_t total_q,
+                                                  int32_t max_q_len, int32_t max_kv_len,
+                                                  int32_t num_splits) {
+    if (batch < 1 || num_heads < 1 || total_q < 1 || max_q_len < 1 || max_kv_len < 1 || num_splits < 0)
+        return 1;
+    return ddt::attn_launched_splits(
+        max_kv_len, noalloc_requested_splits(batch, num_heads, total_q, max_q_len, max_kv_len, num_splits));
+}
 
 extern "C" ddt_status ddt_verify_attn_noalloc(
     const uint16_t *q, const uint16_t *kv_pool, int64_t pool_rows, const int32_t *kv_indices,
@@ -70,19 +91,10 @@ extern "C" ddt_status ddt_verify_attn_noalloc(
     void *scratch = scratch_address();
     if (!err || !scratch) return DDT_ERR_CUDA;
 
-    int splits = num_splits;
-    if (splits == 0) {  // the library's choice, among the counts whose partials fit the scratch
-        int cap = DDT_MAX_SPLITS;
-        while (cap > 1 && ddt_verify_attn_workspace_size(total_q, num_heads, cap) >
-                              (size_t)DDT_NOALLOC_SCRATCH_BYTES)
-            --cap;
-        splits = ddt::attn_choose_splits(batch, num_heads, max_q_len, max_kv_len,
-                                         ddt::device_sm_count(), cap);
-    }
-    const int tile = ddt::attn_kv_tile();
-    int split_cols = (max_kv_len + splits - 1) / splits;
-    split_cols = (split_cols + tile - 1) / tile * tile;
-    splits = (max_kv_len + split_cols - 1) / split_cols;
+    int split_cols = 0, splits = 1;
+    ddt::attn_split_layout(max_kv_len, noalloc_requested_splits(batch, num_heads, total_q, max_q_len,
+                                                                max_kv_len, num_splits),
+                           &split_cols, &splits);
 
     ddt::AttnArgs a;
     memset(&a, 0, sizeof a);

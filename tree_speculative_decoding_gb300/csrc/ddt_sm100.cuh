@@ -132,22 +132,14 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
 }
 
 // ---------------------------------------------------------------- TMA
-// 2-D tile load of box {64 elements, 1 row} at (x, y) into shared memory.
+// 2-D tile load of the map's box at element coordinates (x, y) into shared
+// memory; the box bytes complete on `bar` (rows past the tensor read as 0).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-// four rows (y0..y3) of 64 elements at column x, landing in 4 consecutive 128-byte lines
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int y0,
-                                            int y1, int y2, int y3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
         : "memory");
 }
 
@@ -197,6 +189,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+// copy a 128-row x 256-bit matrix (16 bf16 per row, described by a shared-
+// memory descriptor) into 8 tensor-memory columns of lanes 0-127; ordered with
+// the MMAs that the same thread issues afterwards
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(

@@ -42,6 +42,8 @@ def _load():
         "ddt_compile_visibility": ([P, P, P, P, i32, i32, P, P], i32),
         "ddt_build_tree_visibility": ([P, P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P], i32),
         "ddt_verify_attn_num_splits": ([i32, i32, i32, i32, i32], i32),
+        "ddt_verify_attn_launched_splits": ([i32, i32], i32),
+        "ddt_verify_attn_noalloc_splits": ([i32, i32, i32, i32, i32, i32], i32),
         "ddt_verify_attn_workspace_size": ([i32, i32, i32], sz),
         "ddt_verify_attn": ([P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P,
                              sz, P], i32),
@@ -166,8 +168,53 @@ def ddt_verify_attn_num_splits(batch, num_heads, max_q_len, max_kv_len, num_sms=
     return lib.ddt_verify_attn_num_splits(batch, num_heads, max_q_len, max_kv_len, num_sms)
 
 
+def ddt_verify_attn_launched_splits(max_kv_len, num_splits):
+    """Splits a ddt_verify_attn call with num_splits (>= 1) launches (the
+    requested count rounded to whole 64-column tiles)."""
+    return lib.ddt_verify_attn_launched_splits(int(max_kv_len), int(num_splits))
+
+
+def ddt_verify_attn_noalloc_splits(batch, num_heads, total_q, max_q_len, max_kv_len, num_splits=0):
+    """Splits a ddt_verify_attn_noalloc call with these sizes launches."""
+    return lib.ddt_verify_attn_noalloc_splits(int(batch), int(num_heads), int(total_q),
+                                              int(max_q_len), int(max_kv_len), int(num_splits))
+
+
 def ddt_verify_attn_workspace_size(total_q, num_heads, num_splits):
     return lib.ddt_verify_attn_workspace_size(total_q, num_heads, num_splits)
+
+
+def _attn_args(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_indptr, out, lse,
+               max_q_len, max_kv_len):
+    """The checks both attention entry points need (the C ABI cannot see tensor
+    shapes): dtypes, contiguity, 576-wide rows, out [total_q, H, 512], lse
+    [total_q, H]; returns (total_q, H, batch, max_q_len, max_kv_len)."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(kv_pool, torch.bfloat16, "kv_pool")
+    _dev(out, torch.float32, "out")
+    for n, t in (("kv_indices", kv_indices), ("kv_indptr", kv_indptr), ("qo_indptr", qo_indptr),
+                 ("mask_indptr", mask_indptr)):
+        _dev(t, torch.int32, n)
+    if not (mask.is_cuda and mask.dtype in (torch.int32, torch.uint32) and mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous CUDA 32-bit tensor")
+    if q.dim() != 3 or kv_pool.dim() != 2:
+        raise ValueError("q must be [total_q, H, 576] and kv_pool [pool_rows, 576]")
+    total_q, H, d = q.shape
+    if d != D or kv_pool.shape[-1] != D or tuple(out.shape) != (total_q, H, DL):
+        raise ValueError("q/kv_pool rows must be 576 wide and out [total_q, H, 512]")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+        if tuple(lse.shape) != (total_q, H):
+            raise ValueError("lse must be [total_q, H]")
+    B = qo_indptr.numel() - 1
+    if kv_indptr.numel() != B + 1 or mask_indptr.numel() != B + 1:
+        raise ValueError("qo_indptr, kv_indptr and mask_indptr must all hold batch + 1 entries")
+    if max_q_len is None or max_kv_len is None:
+        qo = qo_indptr.cpu()
+        kv = kv_indptr.cpu()
+        max_q_len = int((qo[1:] - qo[:-1]).max())
+        max_kv_len = int((kv[1:] - kv[:-1]).max())
+    return total_q, H, B, int(max_q_len), int(max_kv_len)
 
 
 def ddt_verify_attn(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_indptr, scale,
@@ -177,21 +224,9 @@ def ddt_verify_attn(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, mask_ind
 
     max_q_len / max_kv_len are host-side bounds used to size the grid; when
     omitted they are read from the indptrs (a device->host copy)."""
-    _dev(q, torch.bfloat16, "q")
-    _dev(kv_pool, torch.bfloat16, "kv_pool")
-    _dev(out, torch.float32, "out")
-    for n, t in (("kv_indices", kv_indices), ("kv_indptr", kv_indptr), ("qo_indptr", qo_indptr),
-                 ("mask_indptr", mask_indptr)):
-        _dev(t, torch.int32, n)
-    total_q, H, d = q.shape
-    if d != D or kv_pool.shape[-1] != D or tuple(out.shape) != (total_q, H, DL):
-        raise ValueError("q/kv_pool rows must be 576 wide and out [total_q, H, 512]")
-    B = qo_indptr.numel() - 1
-    if max_q_len is None or max_kv_len is None:
-        qo = qo_indptr.cpu()
-        kv = kv_indptr.cpu()
-        max_q_len = int((qo[1:] - qo[:-1]).max())
-        max_kv_len = int((kv[1:] - kv[:-1]).max())
+    total_q, H, B, max_q_len, max_kv_len = _attn_args(q, kv_pool, kv_indices, kv_indptr, qo_indptr,
+                                                      mask, mask_indptr, out, lse, max_q_len,
+                                                      max_kv_len)
     if workspace is None:
         splits = num_splits or ddt_verify_attn_num_splits(B, H, max_q_len, max_kv_len)
         nbytes = ddt_verify_attn_workspace_size(total_q, H, splits)
@@ -218,16 +253,9 @@ def ddt_verify_attn_noalloc(q, kv_pool, kv_indices, kv_indptr, qo_indptr, mask, 
     array.  num_splits = 0 takes the library's choice among the counts that
     fit the array; an explicit count that needs more scratch than the array
     holds raises DDTError(DDT_ERR_WORKSPACE)."""
-    _dev(q, torch.bfloat16, "q")
-    _dev(kv_pool, torch.bfloat16, "kv_pool")
-    _dev(out, torch.float32, "out")
-    total_q, H, _ = q.shape
-    B = qo_indptr.numel() - 1
-    if max_q_len is None or max_kv_len is None:
-        qo = qo_indptr.cpu()
-        kv = kv_indptr.cpu()
-        max_q_len = int((qo[1:] - qo[:-1]).max())
-        max_kv_len = int((kv[1:] - kv[:-1]).max())
+    total_q, H, B, max_q_len, max_kv_len = _attn_args(q, kv_pool, kv_indices, kv_indptr, qo_indptr,
+                                                      mask, mask_indptr, out, lse, max_q_len,
+                                                      max_kv_len)
     _check("ddt_verify_attn_noalloc", lib.ddt_verify_attn_noalloc(
         _p(q), _p(kv_pool), kv_pool.shape[0], _p(kv_indices), _p(kv_indptr), _p(qo_indptr),
         _p(mask), _p(mask_indptr), B, H, total_q, int(max_q_len), int(max_kv_len), float(scale),

@@ -96,6 +96,8 @@ class VerifyStep:
 
         self.num_splits = num_splits or ddt.ddt_verify_attn_num_splits(
             self.B, self.H, self.max_q_len, self.max_kv_len)
+        # what the attention launches: the requested count rounded to whole kv tiles
+        self.launched_splits = ddt.ddt_verify_attn_launched_splits(self.max_kv_len, self.num_splits)
         nbytes = ddt.ddt_verify_attn_workspace_size(T, self.H, self.num_splits)
         self.workspace = (torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None)
 
@@ -183,8 +185,10 @@ class VerifyStep:
 
     @property
     def launches_per_step(self):
-        """Kernels one run() launches: tree (+ mask), mask, attention (+ combine), accept."""
-        attn = 2 if self.num_splits > 1 else 1
+        """Kernels one run() or run_one_call() launches: tree + mask (two launches
+        for run() with fused_tree_mask=False), attention partial (+ combine when
+        it splits), accept."""
+        attn = 2 if self.launched_splits > 1 else 1
         return (1 if self.fused_tree_mask else 2) + attn + 1
 
     def run(self, stream=None):
