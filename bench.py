@@ -19,8 +19,10 @@ same path, are printed beside it.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
     python bench.py --timeline [--workload W]   # per-kernel offsets inside a step
 
-For N > 1 (torchrun) every rank runs its own copy of the workload (weak
-scaling, no collective on the data path); the time is the max over ranks.
+For N > 1 every rank runs its own copy of the workload (weak scaling, no
+collective on the data path); the time is the max over ranks.  Under torchrun
+the ranks come from its environment; without it, ``--gpus N`` starts the N
+ranks itself (one process per GPU, rendezvous on 127.0.0.1).
 """
 from __future__ import annotations
 
@@ -178,10 +180,10 @@ def run_device(args, rank, world, local_rank):
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
 
     dist = None
+    torch.cuda.set_device(local_rank)
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
 
     wl = workloads.preset(args.workload)
@@ -583,6 +585,28 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def _free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def launch_ranks(n, argv):
+    """Runs this script as n ranks (RANK / LOCAL_RANK / WORLD_SIZE / MASTER_* set
+    as torchrun sets them) and returns the first non-zero exit code, else 0.
+    Rank 0's JSON line reaches stdout unchanged; the other ranks print none."""
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()),
+               WORLD_SIZE=str(n), LOCAL_WORLD_SIZE=str(n))
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv],
+                              env=dict(env, RANK=str(r), LOCAL_RANK=str(r)))
+             for r in range(n)]
+    codes = [p.wait() for p in procs]
+    return next((c for c in codes if c != 0), 0)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -605,6 +629,10 @@ def main(argv=None):
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv)))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

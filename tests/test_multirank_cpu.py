@@ -63,3 +63,22 @@ def test_bench_rejects_fewer_than_three_warmup_steps():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--steps", "1", "--warmup", "2"])
+
+
+def test_gpus_n_without_torchrun_starts_n_ranks():
+    # --gpus 2 with no torchrun environment: bench.py starts both ranks itself;
+    # the reference arm runs on rank 0 and reports the world size
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
