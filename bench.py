@@ -252,13 +252,15 @@ def run_device(args, rank, world, local_rank):
     elapsed = sum(step_ms) / 1e3
     elapsed_max, flops_all = reduce_over_ranks(elapsed, flops * args.steps, dist)
 
-    # end to end through host buffers: the step's inputs (one packed buffer) from
-    # pinned host memory, the same graph, then the step's results (one packed
-    # buffer) back to pinned host memory -- one copy each way
+    # end to end through host buffers, one C-ABI call per step: a library-owned
+    # graph (ddt_step_graph_create_io) that copies the step's inputs (one packed
+    # buffer) from pinned host memory, runs the step and copies its results (one
+    # packed buffer) back to pinned host memory
     h_in = st.inputs.buf.cpu().pin_memory()
     h_out = torch.empty_like(st.outputs.buf, device="cpu").pin_memory()
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
+    io_graph = st.step_graph(host_io=(h_in, h_out))
     e2e_steps = max(10, args.steps // 10)
     e2e_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
               for _ in range(e2e_steps)]
@@ -266,13 +268,12 @@ def run_device(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             flush.zero_()
             e2e_ev[i][0].record(stream)
-            st.inputs.buf.copy_(h_in, non_blocking=True)
-            graph.replay()
-            h_out.copy_(st.outputs.buf, non_blocking=True)
+            io_graph.launch(stream)
             e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
     st.check_device_errors()
+    io_graph.close()
 
     if rank != 0:
         if dist is not None:
@@ -319,7 +320,9 @@ def run_device(args, rank, world, local_rank):
                      "frac_of_sustained": round(achieved / tf_sus, 4)},
         "e2e": {"value": round(flops / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "call": "ddt_step_graph_launch of a ddt_step_graph_create_io graph: pinned host "
+                        "inputs -> step -> pinned host results, L2 flushed before each"},
         "gpu_launches": launches_per_step * args.steps,
         "accept_sampled": {"ms": round(sampled_ms, 5), "timing": "ddt_tree_links + "
                            "ddt_accept_sampled after the step (temperature 1, no top-k, vocab "
@@ -329,7 +332,8 @@ def run_device(args, rank, world, local_rank):
                       "median"},
         "degenerate": dict(degenerate, timing="each graph replayed on its own after the step, "
                            "L2 flushed, median; autoregressive = the whole step at budget 0, "
-                           "prefill = causal mask compile + attention for 128 new tokens"),
+                           "prefill = ddt_prefill_step (causal chain + mask, attention) for "
+                           "128 new tokens"),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -419,7 +423,7 @@ def time_degenerate(dev, stream, flush, reps=200):
     """The path's degenerate shapes, one request after a prefix of 4096 at 64
     heads: the autoregressive step (budget 0; tree, mask, attention and
     accept) and a prefill chunk of 128 new tokens under a causal mask (the
-    tree replaced by a chain; mask compile and attention)."""
+    tree replaced by a chain: ddt_prefill_step, chain + mask and attention)."""
     import torch
     from tree_speculative_decoding_gb300 import workloads
     from tree_speculative_decoding_gb300.metrics import attn_flops, kv_bytes
@@ -429,11 +433,8 @@ def time_degenerate(dev, stream, flush, reps=200):
         wl = workloads.preset(name)
         st = VerifyStep(wl, dev)
         if name.startswith("prefill"):
-            st.set_causal_chain()
-
             def body(s, st=st):
-                st.compile_visibility(stream=s)
-                st.verify_attn(stream=s)
+                st.run_prefill(stream=s)
         else:
             def body(s, st=st):
                 st.run_one_call(stream=s)

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define DDT_ABI_VERSION 2
+#define DDT_ABI_VERSION 3
 
 /* Sizes fixed by the absorbed-MLA layout ("The 30-Column Mask", shapes log:
  * Dl=512, Dr=64; "The Forward Pass Pseudocode": scores over c_kv and k_pe,
@@ -180,6 +180,30 @@ ddt_status ddt_build_tree_visibility(const float *topk_logp, const int32_t *topk
                                      const int32_t *mask_indptr, int32_t batch, int32_t max_depth,
                                      int32_t topk, int32_t *node_token, int32_t *parent,
                                      int32_t *depth, uint32_t *mask, void *stream);
+
+/*
+ * ddt_build_chain_visibility -- the tree of a prefill chunk and its mask.
+ * Page: "The Architecture of a Speculative Decoding Engine", section "The Core
+ * Design Problem: A Unified Forward Pass": prefill, decode and tree verify are
+ * one forward that differs only in its mask.  For a chunk of q_len_b new
+ * tokens after prefix_len_b cached ones, the tree is the chain
+ * parent[i] = i - 1 (parent[0] = -1), depth[i] = i, request-local indices as
+ * in ddt_build_tree, and its visibility mask is the causal one: row i sees
+ * columns 0 .. prefix_len_b + i.  The mask equals, bit for bit, what
+ * ddt_compile_visibility writes for that chain.
+ *
+ *   qo_indptr, prefix_len, mask_indptr (device) as for ddt_compile_visibility;
+ *              1 <= q_len_b <= 128.
+ *   parent, depth (device) int32 [qo_indptr[batch]] outputs.
+ *   mask       (device) uint32 [mask_indptr[batch]] output.
+ * One launch, no host synchronisation: it can be captured in a CUDA graph.
+ * A request whose q_len is out of range or whose mask range is not
+ * q_len * W words latches DDT_DEVERR_MASK_INDPTR and its mask is not written
+ * (its chain is still written when q_len is in range).
+ */
+ddt_status ddt_build_chain_visibility(const int32_t *qo_indptr, const int32_t *prefix_len,
+                                      const int32_t *mask_indptr, int32_t batch, int32_t *parent,
+                                      int32_t *depth, uint32_t *mask, void *stream);
 
 /*
  * Split-KV sizing.  ddt_verify_attn_num_splits() returns the split count the
@@ -488,6 +512,23 @@ typedef struct {
 ddt_status ddt_verify_step(const ddt_step_args *args, void *stream);
 
 /*
+ * ddt_prefill_step -- one prefill chunk as one call: ddt_build_chain_visibility
+ * then the attention of ddt_verify_attn under that causal mask, on `stream`.
+ * Page: "The Architecture of a Speculative Decoding Engine", section "The Core
+ * Design Problem: A Unified Forward Pass" (prefill is the verify forward with
+ * a causal mask).  It reads the fields of `args` that those two calls take
+ * (layout, indptrs, attention inputs, workspace) and writes parent, depth,
+ * mask, out and lse; the tree inputs, target_argmax and the accept and commit
+ * outputs are not read.  The new tokens' latents must already sit at kv
+ * columns prefix_len_b .. prefix_len_b + q_len_b - 1 (the chunk's own cache
+ * rows); no commit follows, because a chain's accepted path is the identity.
+ * Like the verify step, the attention knows the mask's shape (every prefix
+ * column visible, none after the row's own token) and reads no mask word for
+ * prefix blocks.  Returns the first non-OK status of the two calls.
+ */
+ddt_status ddt_prefill_step(const ddt_step_args *args, void *stream);
+
+/*
  * A CUDA graph of one ddt_verify_step, owned by the library: create captures
  * the step's launches once (the buffers in `args` must then stay allocated and
  * keep their sizes: the verify buffers are sized for budget+1 tokens per
@@ -499,6 +540,20 @@ ddt_status ddt_verify_step(const ddt_step_args *args, void *stream);
  */
 typedef struct ddt_step_graph ddt_step_graph;
 ddt_status ddt_step_graph_create(const ddt_step_args *args, ddt_step_graph **graph);
+/*
+ * ddt_step_graph_create_io -- the same graph with the step's host traffic in
+ * it: a copy of `in_bytes` from h_in to d_in before the step and a copy of
+ * `out_bytes` from d_out to h_out after it, so that one launch takes a step's
+ * inputs from host memory and returns its results there.  h_in and h_out are
+ * pinned host memory (cudaHostAlloc or registered), d_in and d_out device
+ * memory that the caller lays out so that the step's inputs and results fall
+ * inside them (one packed buffer each way); all four stay allocated for the
+ * graph's life.  A size of 0 omits that copy.  Returns DDT_ERR_INVALID_ARG
+ * for a null or unpinned host buffer, else as ddt_step_graph_create.
+ */
+ddt_status ddt_step_graph_create_io(const ddt_step_args *args, const void *h_in, void *d_in,
+                                    size_t in_bytes, void *h_out, const void *d_out,
+                                    size_t out_bytes, ddt_step_graph **graph);
 ddt_status ddt_step_graph_launch(ddt_step_graph *graph, void *stream);
 ddt_status ddt_step_graph_destroy(ddt_step_graph *graph);
 

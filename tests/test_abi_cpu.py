@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.ddt_abi_version() == 2
+    assert lib.ddt_abi_version() == 3
     assert lib.ddt_status_string(0) == b"ok"
     assert b"workspace" in lib.ddt_status_string(3)
 
@@ -174,6 +174,11 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.ddt_verify_attn_noalloc(dummy, ctypes.c_void_p(18), *na[2:], 1, 8, 9, 9, 30, 0.1,
                                        0, dummy, None, None) == 1   # misaligned kv_pool
     assert lib.ddt_verify_step(None, None) == 1
+    assert lib.ddt_prefill_step(None, None) == 1
+    assert lib.ddt_build_chain_visibility(None, dummy, dummy, 1, dummy, dummy, dummy, None) == 1
+    assert lib.ddt_build_chain_visibility(dummy, dummy, dummy, 1, dummy, dummy, None, None) == 1
+    assert lib.ddt_build_chain_visibility(dummy, dummy, dummy, -1, dummy, dummy, dummy, None) == 1
+    assert lib.ddt_build_chain_visibility(dummy, dummy, dummy, 0, dummy, dummy, dummy, None) == 0
     assert lib.ddt_step_graph_create(None, None) == 1
     assert lib.ddt_step_graph_launch(None, None) == 1
     assert lib.ddt_step_graph_destroy(None) == 1

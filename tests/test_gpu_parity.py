@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from tree_speculative_decoding_gb300 import workloads
+from tree_speculative_decoding_gb300 import ddt, workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -292,6 +292,31 @@ def test_step_graph_with_commit_equals_the_staged_commit():
     assert st.accept_len.max().item() > 1
 
 
+def test_step_graph_with_host_copies_returns_the_step_in_host_memory():
+    # ddt_step_graph_create_io: the inputs come from pinned host memory and the
+    # results land there, equal to the staged calls' device results
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.preset("tiny_p21_b8_h8")
+    st, _ = _full_check(wl, n_rows=64)
+    st2 = VerifyStep(wl, "cuda:0")
+    h_in = st2.inputs.buf.cpu().pin_memory()
+    h_out = torch.zeros_like(st2.outputs.buf, device="cpu").pin_memory()
+    st2.inputs.buf.zero_()                         # the graph's own copy must bring them back
+    g = st2.step_graph(host_io=(h_in, h_out))
+    for _ in range(2):
+        g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    for name in ("out", "lse", "accept_len", "accepted_nodes", "commit_tokens", "bonus"):
+        v = st2.outputs.views[name]
+        off = v.data_ptr() - st2.outputs.buf.data_ptr()
+        got = h_out[off:off + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+        assert torch.equal(got, getattr(st, name).cpu()), name
+    g.close()
+    with pytest.raises(ValueError):                # pageable host memory is refused
+        st2.step_graph(host_io=(st2.inputs.buf.cpu(), h_out))
+
+
 def test_step_graph_reports_a_host_check_and_makes_no_graph():
     from tree_speculative_decoding_gb300 import ddt
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
@@ -319,17 +344,25 @@ def test_chain_tree_equals_causal_prefill():
     assert dep.tolist() == list(range(8))
 
 
-def _causal_chunk(wl):
-    """The step's tree replaced by a causal chain, then the mask and the
-    attention: a prefill chunk of q_len tokens after each prefix."""
+def _causal_chunk(wl, one_call=True):
+    """A prefill chunk of q_len tokens after each prefix: the tree replaced by
+    the causal chain on the device, then the attention.  one_call: the whole
+    chunk through ddt_prefill_step; else ddt_build_chain_visibility followed by
+    the standalone ddt_verify_attn (every mask bit honoured)."""
     st = _step(wl)
-    st.set_causal_chain()
-    st.compile_visibility()
-    st.verify_attn()
+    if one_call:
+        st.run_prefill()
+    else:
+        st.build_chain_visibility()
+        st.verify_attn()
     torch.cuda.synchronize()
     st.check_device_errors()
-    par = st.parent.cpu().numpy()
-    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    # the chain, written on the device: parent[i] = i - 1, depth[i] = i per request
+    par_ref = np.concatenate([np.arange(-1, T - 1) for T in wl.q_len]).astype(np.int32)
+    dep_ref = np.concatenate([np.arange(T) for T in wl.q_len]).astype(np.int32)
+    np.testing.assert_array_equal(st.parent.cpu().numpy(), par_ref)
+    np.testing.assert_array_equal(st.depth.cpu().numpy(), dep_ref)
+    mask, mip = oracle.compile_visibility(par_ref, wl.qo_indptr, wl.prefix_len)
     got = st.mask.cpu().numpy().view(np.uint32)
     np.testing.assert_array_equal(got, mask)
     # the chain's mask is the causal one: row i of request b sees columns [0, P_b + i]
@@ -343,20 +376,58 @@ def _causal_chunk(wl):
     return st, mask, mip
 
 
+@pytest.mark.parametrize("one_call", [True, False])
 @pytest.mark.parametrize("H", [1, 16])
-def test_prefill_chunk_of_128_tokens_is_causal_attention(H):
+def test_prefill_chunk_of_128_tokens_is_causal_attention(H, one_call):
     # q_len 128 after prefixes 300, 0 and 33 (a ragged word boundary), every row
     wl = workloads.make_workload(f"prefill{H}", 4250 + H, 3, H, [300, 0, 33], [127, 127, 60], 8,
                                  5000, 1.0)
-    st, mask, mip = _causal_chunk(wl)
+    st, mask, mip = _causal_chunk(wl, one_call)
     _check_attn(st, wl, mask, mip, _sample_rows(wl, 10 ** 9))
 
 
 def test_prefill_chunk_full_size():
-    # the timed shape: 128 new tokens after a prefix of 4096, 64 heads, sampled rows
+    # the timed shape: 128 new tokens after a prefix of 4096, 64 heads, every row
     wl = workloads.preset("prefill_p4096_t128_h64")
     st, mask, mip = _causal_chunk(wl)
-    _check_attn(st, wl, mask, mip, _sample_rows(wl, 384))
+    _check_attn(st, wl, mask, mip, _sample_rows(wl, 10 ** 9))
+
+
+def test_prefill_chunk_graph_replay_matches_the_direct_call():
+    # the chunk is one capturable call: a CUDA graph of ddt_prefill_step replays
+    # to the same bits as the direct call
+    wl = workloads.make_workload("prefill_graph", 4270, 2, 8, [100, 7], [127, 40], 8, 2000, 1.0)
+    st, _, _ = _causal_chunk(wl)
+    ref = st.out.clone(), st.lse.clone(), st.mask.clone()
+    for t in (st.out, st.lse, st.mask, st.parent, st.depth):
+        t.fill_(0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            st.run_prefill(stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    assert torch.equal(st.out, ref[0]) and torch.equal(st.lse, ref[1])
+    assert torch.equal(st.mask, ref[2])
+
+
+def test_chain_rejects_a_wrong_mask_range():
+    # a mask_indptr that is not q_len * W words latches the mask bit; nothing faults
+    wl = workloads.make_workload("chain_bad", 4280, 2, 4, [64, 10], [20, 9], 4, 300, 1.0)
+    st = _step(wl)
+    bad = st.mask_indptr.clone()
+    bad[1] += 1
+    st.mask.fill_(0x55)
+    ddt.ddt_build_chain_visibility(st.qo_indptr, st.prefix_len, bad, st.parent, st.depth, st.mask)
+    torch.cuda.synchronize()
+    status, bits = ddt.ddt_get_error()
+    assert status != 0 and bits & 0x8
+    assert bool((st.mask == 0x55).all())  # neither request's mask range was written
 
 
 def test_autoregressive_steps_budget_zero():

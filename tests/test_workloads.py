@@ -76,13 +76,3 @@ def test_degenerate_shapes():
     pf = w.preset("prefill_p4096_t128_h64", fill_pool=False)
     assert pf.q_len.tolist() == [128] and pf.kv_len.tolist() == [4096 + 128]
     assert w.preset_seed("ar_p4096_b0_h64") != w.preset_seed("prefill_p4096_t128_h64")
-
-
-def test_causal_chain_replaces_the_tree():
-    # host side of VerifyStep only: the chain each request gets in place of its tree
-    from tree_speculative_decoding_gb300.pipeline import VerifyStep
-    wl = w.make_workload("chain_host", 1, 3, 4, [10, 0, 5], [3, 0, 6], 4, 100, 1.0)
-    st = VerifyStep(wl, "cpu")
-    st.set_causal_chain()
-    assert st.parent.tolist() == [-1, 0, 1, 2, -1, -1, 0, 1, 2, 3, 4, 5]
-    assert st.depth.tolist() == [0, 1, 2, 3, 0, 0, 1, 2, 3, 4, 5, 6]

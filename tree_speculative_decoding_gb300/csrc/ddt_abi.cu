@@ -151,6 +151,20 @@ ddt_status ddt_build_tree_visibility(const float *topk_logp, const int32_t *topk
     return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
 }
 
+ddt_status ddt_build_chain_visibility(const int32_t *qo_indptr, const int32_t *prefix_len,
+                                      const int32_t *mask_indptr, int32_t batch, int32_t *parent,
+                                      int32_t *depth, uint32_t *mask, void *stream) {
+    if (!qo_indptr || !prefix_len || !mask_indptr || !parent || !depth || !mask || batch < 0)
+        return DDT_ERR_INVALID_ARG;
+    if (batch == 0) return DDT_OK;
+    DeviceState *st = device_state();
+    if (!st) return DDT_ERR_CUDA;
+    cudaError_t e = ddt::launch_build_chain_visibility(qo_indptr, prefix_len, mask_indptr, batch,
+                                                       parent, depth, mask, st->err,
+                                                       as_stream(stream));
+    return e == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 int32_t ddt_verify_attn_num_splits(int32_t batch, int32_t num_heads, int32_t max_q_len,
                                    int32_t max_kv_len, int32_t num_sms) {
     if (batch < 1 || num_heads < 1 || max_q_len < 1 || max_kv_len < 1) return 1;
@@ -374,11 +388,47 @@ ddt_status ddt_verify_step(const ddt_step_args *a, void *stream) {
                          stream);
 }
 
+ddt_status ddt_prefill_step(const ddt_step_args *a, void *stream) {
+    if (!a) return DDT_ERR_INVALID_ARG;
+    ddt_status st = ddt_build_chain_visibility(a->qo_indptr, a->prefix_len, a->mask_indptr,
+                                               a->batch, a->parent, a->depth, a->mask, stream);
+    if (st != DDT_OK) return st;
+    // the causal chain's mask was just built here: every prefix column is
+    // visible and no row sees a column after its own token
+    return verify_attn_impl(a->q, a->kv_pool, a->pool_rows, a->kv_indices, a->kv_indptr,
+                            a->qo_indptr, a->mask, a->mask_indptr, a->batch, a->num_heads,
+                            a->total_q, a->max_q_len, a->max_kv_len, a->scale, a->num_splits,
+                            a->out, a->lse, a->workspace, a->workspace_bytes, stream, 1);
+}
+
 struct ddt_step_graph {
     cudaGraphExec_t exec = nullptr;
 };
 
-ddt_status ddt_step_graph_create(const ddt_step_args *a, ddt_step_graph **graph) {
+}  // extern "C"
+
+namespace {
+struct StepIO {
+    const void *h_in = nullptr;
+    void *d_in = nullptr;
+    size_t in_bytes = 0;
+    void *h_out = nullptr;
+    const void *d_out = nullptr;
+    size_t out_bytes = 0;
+};
+
+bool is_pinned_host(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // pageable memory on older runtimes reports an error
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
+// Captures [H2D copy] -> ddt_verify_step -> [D2H copy] on a private stream and
+// instantiates it.
+ddt_status step_graph_create(const ddt_step_args *a, const StepIO &io, ddt_step_graph **graph) {
     if (!a || !graph) return DDT_ERR_INVALID_ARG;
     *graph = nullptr;
     if (!device_state()) return DDT_ERR_CUDA;  // one-time set-up outside the capture
@@ -387,7 +437,14 @@ ddt_status ddt_step_graph_create(const ddt_step_args *a, ddt_step_graph **graph)
     ddt_status st = DDT_ERR_CUDA;
     cudaGraph_t g = nullptr;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
-        st = ddt_verify_step(a, s);
+        st = DDT_OK;
+        if (io.in_bytes &&
+            cudaMemcpyAsync(io.d_in, io.h_in, io.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            st = DDT_ERR_CUDA;
+        if (st == DDT_OK) st = ddt_verify_step(a, s);
+        if (st == DDT_OK && io.out_bytes &&
+            cudaMemcpyAsync(io.h_out, io.d_out, io.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            st = DDT_ERR_CUDA;
         const cudaError_t e = cudaStreamEndCapture(s, &g);  // ends the capture on every path
         if (st == DDT_OK && e != cudaSuccess) st = DDT_ERR_CUDA;
     }
@@ -407,6 +464,33 @@ ddt_status ddt_step_graph_create(const ddt_step_args *a, ddt_step_graph **graph)
     h->exec = exec;
     *graph = h;
     return DDT_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ddt_status ddt_step_graph_create(const ddt_step_args *a, ddt_step_graph **graph) {
+    return step_graph_create(a, StepIO{}, graph);
+}
+
+ddt_status ddt_step_graph_create_io(const ddt_step_args *a, const void *h_in, void *d_in,
+                                    size_t in_bytes, void *h_out, const void *d_out,
+                                    size_t out_bytes, ddt_step_graph **graph) {
+    if (!a || !graph) return DDT_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if ((in_bytes && (!h_in || !d_in)) || (out_bytes && (!h_out || !d_out)))
+        return DDT_ERR_INVALID_ARG;
+    if (!device_state()) return DDT_ERR_CUDA;
+    if ((in_bytes && !is_pinned_host(h_in)) || (out_bytes && !is_pinned_host(h_out)))
+        return DDT_ERR_INVALID_ARG;
+    StepIO io;
+    io.h_in = h_in;
+    io.d_in = d_in;
+    io.in_bytes = in_bytes;
+    io.h_out = h_out;
+    io.d_out = d_out;
+    io.out_bytes = out_bytes;
+    return step_graph_create(a, io, graph);
 }
 
 ddt_status ddt_step_graph_launch(ddt_step_graph *graph, void *stream) {

@@ -59,6 +59,10 @@ cudaError_t launch_build_tree_visibility(const float *topk_logp, const int32_t *
                                          const int32_t *prefix_len, const int32_t *mask_indptr,
                                          int32_t *node_token, int32_t *parent, int32_t *depth,
                                          uint32_t *mask, unsigned int *err, cudaStream_t s);
+cudaError_t launch_build_chain_visibility(const int32_t *qo_indptr, const int32_t *prefix_len,
+                                          const int32_t *mask_indptr, int batch, int32_t *parent,
+                                          int32_t *depth, uint32_t *mask, unsigned int *err,
+                                          cudaStream_t s);
 cudaError_t launch_compile_visibility(const int32_t *parent, const int32_t *qo_indptr,
                                       const int32_t *prefix_len, const int32_t *mask_indptr,
                                       int batch, int total_words, uint32_t *mask,

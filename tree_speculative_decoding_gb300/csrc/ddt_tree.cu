@@ -296,6 +296,51 @@ build_tree_visibility_kernel(const float *__restrict__ topk_logp,
     }
 }
 
+// A prefill chunk's tree: the chain parent[i] = i - 1, depth[i] = i, and its
+// mask, which is the causal one: row i sees columns [0, P + i].  Engine page,
+// "The Core Design Problem: A Unified Forward Pass" (prefill, decode and tree
+// verify are one forward that differs only in its mask).  One CTA per
+// request; no parent walk is needed, each word follows from its row and
+// column range alone.
+constexpr int kChainThreads = 256;
+__global__ void __launch_bounds__(kChainThreads)
+build_chain_visibility_kernel(const int32_t *__restrict__ qo_indptr,
+                              const int32_t *__restrict__ prefix_len,
+                              const int32_t *__restrict__ mask_indptr,
+                              int32_t *__restrict__ parent, int32_t *__restrict__ depth,
+                              uint32_t *__restrict__ mask, unsigned int *err) {
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    pdl_trigger();
+    const int base = qo_indptr[b];
+    const int T = qo_indptr[b + 1] - base;
+    const int P = prefix_len[b];
+    const int W = (P + T + 31) >> 5;
+    const int m0 = mask_indptr[b];
+    const bool rows_ok = T >= 1 && T <= DDT_MAX_Q_LEN && base >= 0;
+    const bool mask_ok = rows_ok && P >= 0 && mask_indptr[b + 1] - m0 == T * W;
+    pdl_wait();  // the previous kernel may still read these buffers
+    if (!mask_ok) {
+        if (tid == 0) latch(err, DDT_DEVERR_MASK_INDPTR);
+        if (!rows_ok) return;
+    }
+    for (int i = tid; i < T; i += kChainThreads) {
+        parent[base + i] = i - 1;
+        depth[base + i] = i;
+    }
+    if (!mask_ok) return;
+    for (int w = tid; w < T * W; w += kChainThreads) {
+        const int i = w / W;
+        const int lo = (w - i * W) << 5;  // first column of the word
+        const int last = P + i;           // last visible column of row i
+        uint32_t bits;
+        if (last >= lo + 31) bits = 0xffffffffu;
+        else if (last < lo) bits = 0u;
+        else bits = (2u << (last - lo)) - 1u;  // columns lo .. last
+        mask[m0 + w] = bits;
+    }
+}
+
 // One thread per mask word (grid-stride).  Word w of request b: row
 // i = local / W_b, columns [32k, 32k+32) with k = local % W_b.
 __global__ void compile_visibility_kernel(const int32_t *__restrict__ parent,
@@ -418,7 +463,19 @@ cudaError_t tree_prepare_device() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(build_chain_visibility_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     return e;
+}
+
+cudaError_t launch_build_chain_visibility(const int32_t *qo_indptr, const int32_t *prefix_len,
+                                          const int32_t *mask_indptr, int batch, int32_t *parent,
+                                          int32_t *depth, uint32_t *mask, unsigned int *err,
+                                          cudaStream_t s) {
+    return launch_pdl(build_chain_visibility_kernel, dim3(batch), dim3(kChainThreads), 0, s,
+                      qo_indptr, prefix_len, mask_indptr, parent, depth, mask, err);
 }
 
 cudaError_t launch_build_tree(const float *topk_logp, const int32_t *topk_ids,

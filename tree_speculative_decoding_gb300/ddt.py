@@ -41,6 +41,7 @@ def _load():
         "ddt_mask_indptr": ([P, P, i32, P], i32),
         "ddt_compile_visibility": ([P, P, P, P, i32, i32, P, P], i32),
         "ddt_build_tree_visibility": ([P, P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P], i32),
+        "ddt_build_chain_visibility": ([P, P, P, i32, P, P, P, P], i32),
         "ddt_verify_attn_num_splits": ([i32, i32, i32, i32, i32], i32),
         "ddt_verify_attn_launched_splits": ([i32, i32], i32),
         "ddt_verify_attn_noalloc_splits": ([i32, i32, i32, i32, i32, i32], i32),
@@ -56,7 +57,9 @@ def _load():
         "ddt_get_error": ([P, P], i32),
         "ddt_selftest_wait_timeout": ([ctypes.c_uint32, P], i32),
         "ddt_verify_step": ([P, P], i32),
+        "ddt_prefill_step": ([P, P], i32),
         "ddt_step_graph_create": ([P, P], i32),
+        "ddt_step_graph_create_io": ([P, P, P, sz, P, P, sz, P], i32),
         "ddt_step_graph_launch": ([P, P], i32),
         "ddt_step_graph_destroy": ([P], i32),
     }
@@ -144,6 +147,20 @@ def ddt_compile_visibility(parent, qo_indptr, prefix_len, mask_indptr, mask, str
     B = prefix_len.numel()
     _check("ddt_compile_visibility", lib.ddt_compile_visibility(
         _p(parent), _p(qo_indptr), _p(prefix_len), _p(mask_indptr), B, mask.numel(), _p(mask),
+        _stream(stream)))
+
+
+def ddt_build_chain_visibility(qo_indptr, prefix_len, mask_indptr, parent, depth, mask,
+                               stream=None):
+    """A prefill chunk's chain (parent[i] = i - 1, depth[i] = i) and its causal mask."""
+    for n, t in (("qo_indptr", qo_indptr), ("prefix_len", prefix_len), ("mask_indptr", mask_indptr),
+                 ("parent", parent), ("depth", depth)):
+        _dev(t, torch.int32, n)
+    if not (mask.is_cuda and mask.dtype in (torch.int32, torch.uint32) and mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous CUDA 32-bit tensor")
+    B = prefix_len.numel()
+    _check("ddt_build_chain_visibility", lib.ddt_build_chain_visibility(
+        _p(qo_indptr), _p(prefix_len), _p(mask_indptr), B, _p(parent), _p(depth), _p(mask),
         _stream(stream)))
 
 
@@ -296,14 +313,38 @@ def ddt_verify_step(args: StepArgs, stream=None):
     _check("ddt_verify_step", lib.ddt_verify_step(ctypes.byref(args), _stream(stream)))
 
 
+def ddt_prefill_step(args: StepArgs, stream=None):
+    """One prefill chunk in one call (causal chain + mask, attention)."""
+    _check("ddt_prefill_step", lib.ddt_prefill_step(ctypes.byref(args), _stream(stream)))
+
+
 class StepGraph:
     """A library-owned CUDA graph of one ddt_verify_step; the tensors behind
     `args` must outlive it."""
 
-    def __init__(self, args: StepArgs, keep_alive=()):
-        self._keep = (args, tuple(keep_alive))
+    def __init__(self, args: StepArgs, keep_alive=(), io=None):
+        """io = (h_in, d_in, h_out, d_out): pinned host and device uint8 buffers;
+        the graph then copies h_in -> d_in before the step and d_out -> h_out
+        after it (ddt_step_graph_create_io)."""
+        self._keep = (args, tuple(keep_alive), io)
         h = ctypes.c_void_p()
-        _check("ddt_step_graph_create", lib.ddt_step_graph_create(ctypes.byref(args), ctypes.byref(h)))
+        if io is None:
+            _check("ddt_step_graph_create",
+                   lib.ddt_step_graph_create(ctypes.byref(args), ctypes.byref(h)))
+        else:
+            h_in, d_in, h_out, d_out = io
+            for t, dev, n in ((h_in, False, "h_in"), (d_in, True, "d_in"), (h_out, False, "h_out"),
+                              (d_out, True, "d_out")):
+                if t.is_cuda != dev or not t.is_contiguous() or (not dev and not t.is_pinned()):
+                    raise ValueError(f"{n} must be a contiguous {'CUDA' if dev else 'pinned host'} "
+                                     "tensor")
+            nin = h_in.numel() * h_in.element_size()
+            nout = h_out.numel() * h_out.element_size()
+            if nin > d_in.numel() * d_in.element_size() or nout > d_out.numel() * d_out.element_size():
+                raise ValueError("a host buffer is larger than its device buffer")
+            _check("ddt_step_graph_create_io", lib.ddt_step_graph_create_io(
+                ctypes.byref(args), _p(h_in), _p(d_in), nin, _p(h_out), _p(d_out), nout,
+                ctypes.byref(h)))
         self._h = h
 
     def launch(self, stream=None):

@@ -110,23 +110,20 @@ class VerifyStep:
         ddt.ddt_compile_visibility(self.parent, self.qo_indptr, self.prefix_len, self.mask_indptr,
                                    self.mask, stream)
 
-    def set_causal_chain(self):
+    def build_chain_visibility(self, stream=None):
         """Replaces the tree by a chain, parent[i] = i - 1 (depth i) within each
-        request.  Engine page, "The Core Design Problem: A Unified Forward Pass":
-        prefill, decode and tree verify are one forward that differs only in
-        its mask.  The mask compiled from it is causal over the request's q_len
-        new tokens, so compile_visibility followed by verify_attn is a prefill
-        chunk after the prefix; budget 0 (q_len 1) is the autoregressive step.
-        A blocking host-to-device copy: call it outside stream capture."""
-        par = np.empty(self.total_q, np.int32)
-        dep = np.empty(self.total_q, np.int32)
-        qo = self.wl.qo_indptr
-        for b in range(self.B):
-            lo, hi = int(qo[b]), int(qo[b + 1])
-            par[lo:hi] = np.arange(-1, hi - lo - 1, dtype=np.int32)
-            dep[lo:hi] = np.arange(hi - lo, dtype=np.int32)
-        self.parent.copy_(torch.from_numpy(par))
-        self.depth.copy_(torch.from_numpy(dep))
+        request, and writes its mask, which is causal over the request's q_len
+        new tokens (ddt_build_chain_visibility, one launch).  Engine page, "The
+        Core Design Problem: A Unified Forward Pass": prefill, decode and tree
+        verify are one forward that differs only in its mask, so verify_attn
+        after it is a prefill chunk after the prefix."""
+        ddt.ddt_build_chain_visibility(self.qo_indptr, self.prefix_len, self.mask_indptr,
+                                       self.parent, self.depth, self.mask, stream)
+
+    def run_prefill(self, stream=None):
+        """A prefill chunk as one C call (ddt_prefill_step): chain + causal
+        mask, then the attention."""
+        ddt.ddt_prefill_step(self.step_args(), stream)
 
     def build_tree_visibility(self, stream=None):
         ddt.ddt_build_tree_visibility(self.topk_logp, self.topk_ids, self.root_id, self.budget,
@@ -179,9 +176,15 @@ class VerifyStep:
         """The step as a single C call (ddt_verify_step)."""
         ddt.ddt_verify_step(self.step_args(commit_kv), stream)
 
-    def step_graph(self, commit_kv=False):
-        """A library-owned CUDA graph of the step (ddt_step_graph_*)."""
-        return ddt.StepGraph(self.step_args(commit_kv), keep_alive=(self,))
+    def step_graph(self, commit_kv=False, host_io=None):
+        """A library-owned CUDA graph of the step (ddt_step_graph_*).  host_io =
+        (h_in, h_out), pinned host buffers the size of the input and output
+        arenas: the graph then copies h_in into the inputs before the step and
+        the outputs into h_out after it (ddt_step_graph_create_io)."""
+        io = None
+        if host_io is not None:
+            io = (host_io[0], self.inputs.buf, host_io[1], self.outputs.buf)
+        return ddt.StepGraph(self.step_args(commit_kv), keep_alive=(self,), io=io)
 
     @property
     def launches_per_step(self):
