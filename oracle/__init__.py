@@ -56,7 +56,7 @@ def _load():
             lib.oracle_accept.argtypes = [P, P, P, P, i32, i32, P, P, P, P]
             lib.oracle_commit_kv.argtypes = [P, i64, P, P, P, P, P, i32, i32, P]
             lib.oracle_tree_links.argtypes = [P, P, i32, P, P, P]
-            lib.oracle_accept_sampled.argtypes = [P, P, P, P, i32, P, P, P, i32, i32, i32,
+            lib.oracle_accept_sampled.argtypes = [P, P, P, P, i32, P, P, P, P, i32, i32, i32,
                                                   P, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_build_tree, lib.oracle_mask_indptr,
@@ -220,10 +220,12 @@ def tree_links(parent, qo_indptr):
     return fc, ns, ri
 
 
-def accept_sampled(node_token, parent, qo_indptr, logits, temperature, top_k, coins, max_depth):
+def accept_sampled(node_token, parent, qo_indptr, logits, temperature, top_k, coins, max_depth,
+                   top_p=None):
     """Sampling accept (reading R15).  logits float32 [rows, vocab]; temperature
-    float32 [B]; top_k int32 [B]; coins float32 [rows, coin_stride].  Returns
-    (accept_len, accepted_nodes, commit_tokens, bonus) as accept() does."""
+    float32 [B]; top_k int32 [B]; coins float32 [rows, coin_stride]; top_p
+    float32 [B] or None (no top-p).  Returns (accept_len, accepted_nodes,
+    commit_tokens, bonus) as accept() does."""
     lib = _load()
     node_token = _c(node_token, np.int32)
     parent = _c(parent, np.int32)
@@ -233,13 +235,15 @@ def accept_sampled(node_token, parent, qo_indptr, logits, temperature, top_k, co
     top_k = _c(top_k, np.int32)
     coins = _c(coins, np.float32)
     B = qo_indptr.shape[0] - 1
+    top_p = None if top_p is None else _c(top_p, np.float32)
     W = int(max_depth) + 1
     alen = np.empty(B, np.int32)
     acc = np.empty((B, W), np.int32)
     com = np.empty((B, W), np.int32)
     bon = np.empty(B, np.int32)
     rc = lib.oracle_accept_sampled(_ptr(node_token), _ptr(parent), _ptr(qo_indptr), _ptr(logits),
-                                   int(logits.shape[1]), _ptr(temperature), _ptr(top_k), _ptr(coins),
+                                   int(logits.shape[1]), _ptr(temperature), _ptr(top_k),
+                                   None if top_p is None else _ptr(top_p), _ptr(coins),
                                    int(coins.shape[1]), B, int(max_depth), _ptr(alen), _ptr(acc),
                                    _ptr(com), _ptr(bon))
     if rc != 0:

@@ -38,8 +38,8 @@
  *           Already Working for Linear, Planned for DDTree" -- sampling accept
  *           reuses a tree rejection-sampling kernel that takes the tree as
  *           (retrieve_index, retrieve_next_token, retrieve_next_sibling) and
- *           filters the target with temperature and top-k.  The pages give no
- *           algorithm text; the reading taken is R15 below.
+ *           filters the target with temperature, top-k and top-p.  The pages
+ *           give no algorithm text; the reading taken is R15 below.
  *   [COMMIT] "The Architecture of a Speculative Decoding Engine", the
  *           append-then-compact scheme and "The Final Resolution: A Concrete
  *           Trace" -- every tree node's latent is appended after the
@@ -64,7 +64,12 @@
  *   R15 sampling accept (target-only, deterministic drafts): at node n the
  *       target distribution p is softmax(logits[n] / T) over the tokens whose
  *       logit is at least the top_k-th largest (all of them when top_k <= 0
- *       or >= vocab; ties kept).  The children of n are tried in index order
+ *       or >= vocab; ties kept).  Top-p then keeps the tokens whose logit is
+ *       at least tau, the largest logit x with S(x) >= top_p, where S(x) is
+ *       the mass of p over the tokens whose logit is at least x (the nucleus
+ *       taken in logit order; tokens equal to tau are all kept), and p is
+ *       renormalised over them; top_p outside (0, 1) keeps every token.
+ *       The children of n are tried in index order
  *       against the residual r (p minus the tokens already rejected): child c
  *       with token t is taken when coin[n][i] < r(t) / mass(r), else t leaves
  *       the residual.  With no child taken, the bonus is the first token id v
@@ -470,13 +475,14 @@ static int cmp_desc(const void *a, const void *b) {
 /*
  * [SAMPLE] reading R15.  coins is [rows][coin_stride] uniform [0,1): coin i is
  * for the i-th child tried at that node, the last one for the bonus draw.
- * Outputs as in oracle_accept.
+ * top_p is [B] or NULL (no top-p).  Outputs as in oracle_accept.
  */
 int oracle_accept_sampled(const int32_t *node_token, const int32_t *parent,
                           const int32_t *qo_indptr, const float *logits, int vocab,
-                          const float *temperature, const int32_t *top_k, const float *coins,
-                          int coin_stride, int B, int max_depth, int32_t *accept_len,
-                          int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus) {
+                          const float *temperature, const int32_t *top_k, const float *top_p,
+                          const float *coins, int coin_stride, int B, int max_depth,
+                          int32_t *accept_len, int32_t *accepted_nodes, int32_t *commit_tokens,
+                          int32_t *bonus) {
     int width = max_depth + 1;
     double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
     float *sorted = (float *)malloc(sizeof(float) * (size_t)vocab);
@@ -512,6 +518,30 @@ int oracle_accept_sampled(const int32_t *node_token, const int32_t *parent,
                     z += p[v];
                 }
                 for (int v = 0; v < vocab; ++v) p[v] /= z;
+                double tp = top_p ? (double)top_p[b] : 1.0;
+                if (tp > 0.0 && tp < 1.0) {
+                    /* the kept logits in descending order; walk groups of equal
+                       logits, adding their mass, until the mass reaches top_p */
+                    int m = 0;
+                    for (int v = 0; v < vocab; ++v) if (l[v] >= thr) sorted[m++] = l[v];
+                    qsort(sorted, (size_t)m, sizeof(float), cmp_desc);
+                    double S = 0.0;
+                    float tau = sorted[m - 1];
+                    for (int i = 0; i < m;) {
+                        float x = sorted[i];
+                        double px = exp(((double)x - (double)l[amax]) / (double)temperature[b]) / z;
+                        int j = i;
+                        while (j < m && sorted[j] == x) { S += px; ++j; }
+                        if (S >= tp) { tau = x; break; }
+                        i = j;
+                    }
+                    double z2 = 0.0;
+                    for (int v = 0; v < vocab; ++v) {
+                        if (l[v] < tau) p[v] = 0.0;
+                        z2 += p[v];
+                    }
+                    for (int v = 0; v < vocab; ++v) p[v] /= z2;
+                }
             }
             /* the children, in index order, against the residual; a node needs
                one coin per child plus one for the bonus */

@@ -2,14 +2,17 @@
 
 "The DDTree CUDA Graph Fix ...", section "Temperature Support: Already Working
 for Linear, Planned for DDTree": sampling accept runs tree rejection sampling
-on the target distribution (temperature, top-k), with the tree given as
-(retrieve_index, retrieve_next_token, retrieve_next_sibling).  The pages give
-no algorithm text, so the reading (R15) is pinned by what any correct reading
-must satisfy:
+on the target distribution (temperature, top-k, top-p), with the tree given
+as (retrieve_index, retrieve_next_token, retrieve_next_sibling).  The pages
+give no algorithm text, so the reading (R15) is pinned by what any correct
+reading must satisfy:
 - every emitted token is distributed as the target distribution, a Monte Carlo
-  check against a softmax computed here;
-- at temperature 0 it is the greedy walk;
-- a hand-worked example;
+  check against a softmax computed here, and with top-p against a brute-force
+  nucleus (every distinct logit tried as the threshold);
+- at temperature 0, and for a vanishing top-p, it is the greedy walk; top-p of
+  1 (or outside (0, 1)) is no top-p;
+- hand-worked examples, one where the nucleus changes the walk and one where
+  tied tokens at the threshold are all kept;
 - the links agree with the children sets.
 """
 import numpy as np
@@ -202,3 +205,102 @@ def test_a_one_token_vocabulary_accepts_the_matching_child(oracle_mod):
     assert acc[0].tolist() == [0, 2, 3, -1]
     assert com[0].tolist() == [0, 0, 0, -1]
     assert bon.tolist() == [0]
+
+
+# ------------------------------------------------------------------- top-p
+def _nucleus(l, T, k, top_p):
+    """Brute force of the top-p reading: tau is the largest logit x whose mass
+    S(x) = p(logit >= x) reaches top_p; the tokens at or above tau, renormalised."""
+    p = _softmax_topk(l, T, k)
+    if not 0.0 < top_p < 1.0:
+        return p
+    lv = l.astype(np.float64)
+    for x in sorted(set(lv[p > 0].tolist()), reverse=True):
+        if p[lv >= x].sum() >= top_p:
+            q = np.where(lv >= x, p, 0.0)
+            return q / q.sum()
+    raise AssertionError("the whole mass never reaches top_p")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_top_p_of_one_or_outside_the_unit_interval_is_no_top_p(oracle_mod, seed):
+    tok, par, qo, logits, coins = _deep_case(seed)
+    t, k = np.array([1.1], np.float32), np.array([0], np.int32)
+    ref = oracle_mod.accept_sampled(tok, par, qo, logits, t, k, coins, 4)
+    for tp in (1.0, 1.5, 0.0, -0.5):
+        got = oracle_mod.accept_sampled(tok, par, qo, logits, t, k, coins, 4,
+                                        top_p=np.array([tp], np.float32))
+        for x, y in zip(got, ref):
+            np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_a_vanishing_top_p_is_the_greedy_walk(oracle_mod, seed):
+    # with distinct logits the nucleus of a tiny top_p is the argmax alone
+    tok, par, qo, logits, coins = _deep_case(seed)
+    got = oracle_mod.accept_sampled(tok, par, qo, logits, np.array([1.3], np.float32),
+                                    np.array([0], np.int32), coins, 4,
+                                    top_p=np.array([1e-6], np.float32))
+    g = oracle_mod.accept(tok, par, qo, logits.argmax(axis=1).astype(np.int32), 4)
+    for x, y in zip(got, g):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_top_p_hand_worked_example(oracle_mod):
+    # vocab 4, T = 1, logits log([1, 2, 1, 4]): p = [1, 2, 1, 4] / 8.  In logit
+    # order the mass reaches 0.5 (token 3), 0.75 (token 1), 1.0 (tokens 0 and 2).
+    # top_p 0.6: tau = log 2, the nucleus is {3, 1} with p = {3: 2/3, 1: 1/3}.
+    # root (token 7): child 1 (token 0) has p 0 and is rejected, the residual
+    # keeps mass 1; child 2 (token 1): a = 1/3, coin 0.3 -> taken.  Node 2 is a
+    # leaf; bonus coin 0.5: cumulative 1/3 at id 1, 1 at id 3 -> token 3.
+    # Without top-p child 1 leaves mass 7/8, child 2 gets a = 2/7 < 0.3 and is
+    # rejected, so the nucleus changes the walk.
+    par = np.array([-1, 0, 0], np.int32)
+    tok = np.array([7, 0, 1], np.int32)
+    logits = np.tile(np.log(np.array([1, 2, 1, 4], np.float32)), (3, 1)).astype(np.float32)
+    coins = np.array([[0.6, 0.3, 0.9], [0.9, 0.9, 0.9], [0.9, 0.9, 0.5]], np.float32)
+    args = (tok, par, np.array([0, 3], np.int32), logits, np.array([1.0], np.float32),
+            np.array([0], np.int32), coins, 3)
+    alen, acc, com, bon = oracle_mod.accept_sampled(*args, top_p=np.array([0.6], np.float32))
+    assert alen.tolist() == [2] and acc[0].tolist() == [0, 2, -1, -1]
+    assert com[0].tolist() == [1, 3, -1, -1] and bon.tolist() == [3]
+    alen0, acc0, com0, bon0 = oracle_mod.accept_sampled(*args)
+    assert alen0.tolist() == [1] and acc0[0].tolist() == [0, -1, -1, -1]
+    # top_p 0.8 needs the tied tokens 0 and 2, and both are kept: no filter at all
+    got = oracle_mod.accept_sampled(*args, top_p=np.array([0.8], np.float32))
+    for x, y in zip(got, (alen0, acc0, com0, bon0)):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("temp,top_k,top_p,kids", [(1.0, 0, 0.7, [2, 5, 0]),
+                                                   (0.8, 5, 0.6, [5, 1]),
+                                                   (1.4, 0, 0.9, [])])
+def test_emitted_tokens_follow_the_nucleus(oracle_mod, temp, top_k, top_p, kids):
+    # as the temperature/top-k check: first and second emitted tokens against the
+    # brute-force nucleus of the root's and the child's logits
+    V, n = 8, 20000
+    rng = np.random.default_rng(11)
+    T = 1 + len(kids)
+    par = np.array([-1] + [0] * len(kids), np.int32)
+    tok = np.array([9] + kids, np.int32)
+    logits = rng.normal(scale=1.5, size=(T, V)).astype(np.float32)
+    B = n
+    coins = rng.random((B * T, 4)).astype(np.float32)
+    alen, acc, com, bon = oracle_mod.accept_sampled(
+        np.tile(tok, B), np.tile(par, B), np.arange(B + 1, dtype=np.int32) * T,
+        np.tile(logits, (B, 1)), np.full(B, temp, np.float32), np.full(B, top_k, np.int32),
+        coins, 2, top_p=np.full(B, top_p, np.float32))
+    p_root = _nucleus(logits[0], temp, top_k, top_p)
+    assert (p_root == 0).any()  # the nucleus removes tokens
+    first = com[:, 0]
+    freq = np.bincount(first, minlength=V) / B
+    assert np.all(freq[p_root == 0] == 0)
+    assert np.abs(freq - p_root).max() < 4.5 * np.sqrt(0.25 / B)
+    for ci, t in enumerate(kids):
+        took = first == t
+        if took.sum() < 2000:
+            continue
+        p_child = _nucleus(logits[1 + ci], temp, top_k, top_p)
+        f2 = np.bincount(com[took, 1], minlength=V) / took.sum()
+        assert np.all(f2[p_child == 0] == 0)
+        assert np.abs(f2 - p_child).max() < 4.5 * np.sqrt(0.25 / took.sum())
