@@ -282,6 +282,7 @@ def run_device(args, rank, world, local_rank):
 
     commit_ms = time_commit(st, stream, flush)
     sampled_ms = time_sampled(st, stream, flush, wl.vocab)
+    sampled_topp_ms = time_sampled(st, stream, flush, wl.vocab, top_p=0.9)
     degenerate = time_degenerate(dev, stream, flush)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     ms_per_step = elapsed_max * 1e3 / args.steps
@@ -324,7 +325,8 @@ def run_device(args, rank, world, local_rank):
                 "call": "ddt_step_graph_launch of a ddt_step_graph_create_io graph: pinned host "
                         "inputs -> step -> pinned host results, L2 flushed before each"},
         "gpu_launches": launches_per_step * args.steps,
-        "accept_sampled": {"ms": round(sampled_ms, 5), "timing": "ddt_tree_links + "
+        "accept_sampled": {"ms": round(sampled_ms, 5), "top_p_0.9_ms": round(sampled_topp_ms, 5),
+                           "timing": "ddt_tree_links + "
                            "ddt_accept_sampled after the step (temperature 1, no top-k, vocab "
                            f"{wl.vocab}, seeded N(0,1.5) logits); graph replay, L2 flushed, median"},
         "commit_kv": {"ms": round(commit_ms, 5), "timing": "ddt_commit_kv alone after the step, each "
@@ -392,9 +394,10 @@ def time_commit(st, stream, flush, reps=200):
     return ms
 
 
-def time_sampled(st, stream, flush, vocab, reps=200):
+def time_sampled(st, stream, flush, vocab, reps=200, top_p=None):
     """Median time of the sampling accept (links + rejection sampling) on the
-    step's tree with seeded target logits, temperature 1 and no top-k."""
+    step's tree with seeded target logits, temperature 1, no top-k, and top-p
+    `top_p` (None: no top-p)."""
     import torch
     from tree_speculative_decoding_gb300 import ddt
     dev = st.node_token.device
@@ -405,13 +408,14 @@ def time_sampled(st, stream, flush, vocab, reps=200):
     coins = torch.rand((rows, st.wl.K + 1), generator=gen, device=dev)
     temp = torch.ones(st.B, dtype=torch.float32, device=dev)
     top_k = torch.zeros(st.B, dtype=torch.int32, device=dev)
+    tp = None if top_p is None else torch.full((st.B,), top_p, dtype=torch.float32, device=dev)
     fc, ns, ri = (torch.empty(rows, dtype=torch.int32, device=dev) for _ in range(3))
     out = [torch.empty_like(t) for t in (st.accept_len, st.accepted_nodes, st.commit_tokens, st.bonus)]
 
     def body(s):
         ddt.ddt_tree_links(st.parent, st.qo_indptr, fc, ns, ri, stream=s)
         ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, logits, temp, top_k, coins,
-                               st.wl.max_depth, *out, stream=s)
+                               st.wl.max_depth, *out, stream=s, top_p=tp)
     with torch.cuda.stream(stream):
         body(stream)
     ms = replay_median(body, stream, flush, reps)

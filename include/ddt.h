@@ -17,7 +17,7 @@
  *   ddt_accept              greedy walk: longest accepted chain + bonus token
  *   ddt_commit_kv           gather the accepted latents after the committed prefix
  *   ddt_tree_links          the tree as first-child / next-sibling links
- *   ddt_accept_sampled      tree rejection sampling with temperature and top-k
+ *   ddt_accept_sampled      tree rejection sampling with temperature, top-k, top-p
  *   ddt_verify_step         tree + mask, attention, accept (+ commit) in one call;
  *                           ddt_step_graph_* hold the same as one CUDA graph
  *
@@ -37,7 +37,7 @@
  *     stage of this ABI writes (tree, mask, split partials) and before its
  *     first write.  Arguments that only the caller writes (q, kv_pool,
  *     kv_indices, the indptr arrays, top-k inputs, target_argmax, and the
- *     sampling accept's temperature, top_k and logits) may be read before
+ *     sampling accept's temperature, top_k, top_p and logits) may be read before
  *     that wait.  Producing them in a kernel that signals early
  *     completion (cudaTriggerProgrammaticLaunchCompletion) and then calling
  *     an entry point right after it is therefore unsupported.  An ordinary
@@ -366,6 +366,10 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
  *     logit is at least the top_k[b]-th largest (ties kept; all tokens when
  *     top_k[b] <= 0 or >= vocab); temperature[b] <= 0 gives one-hot at the
  *     argmax (lowest id on ties);
+ *   - top-p, after top-k: tau is the largest logit x whose mass S(x), the
+ *     mass of p over the tokens with logit >= x, reaches top_p[b]; the tokens
+ *     with logit >= tau are kept (ties at tau all kept) and p is renormalised
+ *     over them.  top_p == NULL, or top_p[b] outside (0, 1), applies none;
  *   - at node n the children are tried in index order against the residual r
  *     (p minus the tokens already rejected at n): child i, with token t, is
  *     taken when coins[n][i] < r(t) / mass(r), otherwise t leaves r;
@@ -374,14 +378,17 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
  * Every emitted token is then distributed as p.  At temperature 0 (or top_k
  * 1) this is exactly ddt_accept with target_argmax = the logits' argmax.
  * Probabilities are fp32 on the device, so a coin within ~1e-6 of a threshold
- * may decide differently from an fp64 evaluation.  If rounding leaves the
+ * may decide differently from an fp64 evaluation.  The top-p set is found
+ * with masses summed in 2^-40 fixed point (the same set on every run); it can
+ * differ from an fp64 evaluation only when S crosses top_p within ~1e-6.  If rounding leaves the
  * bonus target at or above the residual's total, the bonus is a token with
  * residual mass near the end of the id range (the argmax if r is empty).
  *
  *   node_token, first_child, next_sibling, qo_indptr
  *                 (device) the tree (ddt_build_tree) and its links (ddt_tree_links).
  *   target_logits (device) float [qo_indptr[batch]][vocab]: target logits at each node.
- *   temperature   (device) float [batch]; top_k (device) int32 [batch].
+ *   temperature   (device) float [batch]; top_k (device) int32 [batch];
+ *   top_p         (device) float [batch], or NULL.
  *   coins         (device) float [qo_indptr[batch]][coin_stride], uniform in [0,1):
  *                 coin i for the i-th child tried at a node, the last for the
  *                 bonus; coin_stride >= 1 + the largest number of children.
@@ -394,7 +401,8 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
 ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_child,
                               const int32_t *next_sibling, const int32_t *qo_indptr,
                               const float *target_logits, int32_t vocab, const float *temperature,
-                              const int32_t *top_k, const float *coins, int32_t coin_stride,
+                              const int32_t *top_k, const float *top_p, const float *coins,
+                              int32_t coin_stride,
                               int32_t batch, int32_t max_depth, int32_t *accept_len,
                               int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus,
                               void *stream);

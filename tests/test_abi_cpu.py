@@ -155,16 +155,19 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.ddt_commit_kv(dummy, 10, dummy, dummy, dummy, dummy, dummy, 0, 7, None, None) == 0
     assert lib.ddt_tree_links(None, dummy, 1, dummy, dummy, dummy, None) == 1
     sa = [dummy] * 5
-    assert lib.ddt_accept_sampled(*sa, 0, dummy, dummy, dummy, 3, 1, 7, dummy, dummy, dummy, dummy,
+    # (tree, links, qo, logits), vocab, temperature, top_k, top_p (may be NULL), coins,
+    # coin_stride, batch, max_depth, four outputs, stream
+    out4 = [dummy] * 4
+    assert lib.ddt_accept_sampled(*sa, 0, dummy, dummy, None, dummy, 3, 1, 7, *out4,
                                   None) == 1   # vocab 0
-    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 3, 1, 8, dummy, dummy, dummy,
-                                  dummy, None) == 2  # max_depth 8
-    assert lib.ddt_accept_sampled(*sa, 262145, dummy, dummy, dummy, 3, 1, 7, dummy, dummy, dummy,
-                                  dummy, None) == 2  # vocab above DDT_MAX_VOCAB
-    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 0, 1, 7, dummy, dummy, dummy,
-                                  dummy, None) == 1  # no coins
-    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, 3, 0, 7, dummy, dummy, dummy,
-                                  dummy, None) == 0  # empty batch: nothing to do
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, None, dummy, 3, 1, 8, *out4,
+                                  None) == 2  # max_depth 8
+    assert lib.ddt_accept_sampled(*sa, 262145, dummy, dummy, None, dummy, 3, 1, 7, *out4,
+                                  None) == 2  # vocab above DDT_MAX_VOCAB
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, None, dummy, 0, 1, 7, *out4,
+                                  None) == 1  # no coins
+    assert lib.ddt_accept_sampled(*sa, 100, dummy, dummy, dummy, dummy, 3, 0, 7, *out4,
+                                  None) == 0  # empty batch: nothing to do
     # the allocation-free attention makes the same host checks before touching the device
     na = [dummy, dummy, 100, dummy, dummy, dummy, dummy, dummy]
     assert lib.ddt_verify_attn_noalloc(*na, 1, 8, 9, 9, 30, 0.1, 0, None, None, None) == 1

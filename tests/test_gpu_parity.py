@@ -623,7 +623,7 @@ def _links(st):
     return fc, ns, ri
 
 
-def _sampled(st, logits, temp, top_k, coins):
+def _sampled(st, logits, temp, top_k, coins, top_p=None):
     from tree_speculative_decoding_gb300 import ddt
     fc, ns, _ = _links(st)
     B, W = st.accepted_nodes.shape
@@ -634,7 +634,8 @@ def _sampled(st, logits, temp, top_k, coins):
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
     ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, dev(logits, np.float32),
                            dev(temp, np.float32), dev(top_k, np.int32), dev(coins, np.float32),
-                           st.wl.max_depth, *out)
+                           st.wl.max_depth, *out,
+                           top_p=None if top_p is None else dev(top_p, np.float32))
     torch.cuda.synchronize()
     st.check_device_errors()
     return [t.cpu().numpy() for t in out]
@@ -797,6 +798,88 @@ def test_sampled_accept_residual_draw_over_many_steps():
     assert np.all(np.abs(f_step - p_step) < 4.5 * np.sqrt(p_step * (1 - p_step) / B) + 1e-3)
     top = np.argsort(p)[::-1][:5]
     assert np.all(np.abs(freq[top] - p[top]) < 4.5 * np.sqrt(p[top] * (1 - p[top]) / B) + 1e-3)
+
+
+@pytest.mark.parametrize("name,vocab,temp,top_k,top_p,bias,seed", [
+    ("tiny_p21_b8_h8", 512, 0.8, 0, 0.9, 6.0, 12),
+    ("mixed_bs32_b16or32_h16", 32768, 0.5, 0, 0.6, 6.0, 11),
+    ("mixed_bs32_b16or32_h16", 32768, 0.7, 20, 0.7, 5.0, 11),
+    ("tiny_p21_b8_h8", 1001, 0.9, 5, 0.5, 3.0, 48),
+    ("tiny_p21_b8_h8", 1001, 0.6, 0, 0.75, 4.0, 27),
+    ("mixed_bs32_b16or32_h16", 20002, 0.5, 12, 0.8, 5.0, 11),
+    ("tiny_p21_b8_h8", 262144, 0.35, 0, 0.8, 8.0, 12),
+    ("tiny_p21_b8_h8", 262144, 0.35, 64, 0.7, 6.0, 35),
+])
+def test_sampled_accept_top_p_matches_oracle(name, vocab, temp, top_k, top_p, bias, seed):
+    # the kept set is an integer decision taken from a sum of exponentials (fp64
+    # in the oracle, 2^-40 fixed point over fp32 exponentials on the device): the
+    # seeds are ones whose oracle decisions do not move when top_p moves by
+    # +-3e-6 or every coin by +-3e-5, so both sides must decide alike.  In every
+    # case a walk goes past the root and top-p changes some request's outcome.
+    wl = workloads.preset(name)
+    st, tok, par, logits, coins = _sampling_case(wl, vocab, seed, bias)
+    t, k, tp = np.full(wl.B, temp), np.full(wl.B, top_k), np.full(wl.B, top_p, np.float32)
+    ref = oracle.accept_sampled(tok, par, wl.qo_indptr, logits, t, k, coins, wl.max_depth,
+                                top_p=tp)
+    for moved in ([tp - np.float32(3e-6), coins], [tp + np.float32(3e-6), coins],
+                  [tp, np.clip(coins - 3e-5, 0, 0.99999)], [tp, np.clip(coins + 3e-5, 0, 0.99999)]):
+        r = oracle.accept_sampled(tok, par, wl.qo_indptr, logits, t, k, moved[1], wl.max_depth,
+                                  top_p=moved[0])
+        for a, b in zip(r, ref):
+            np.testing.assert_array_equal(a, b)
+    plain = oracle.accept_sampled(tok, par, wl.qo_indptr, logits, t, k, coins, wl.max_depth)
+    assert ref[0].max() > 1
+    assert (ref[0] != plain[0]).any() or (ref[3] != plain[3]).any()
+    got = _sampled(st, logits, t, k, coins, top_p=tp)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+    # top_p 1 (no filter) on the device is the plain sampling accept
+    got1 = _sampled(st, logits, t, k, coins, top_p=np.ones(wl.B, np.float32))
+    got0 = _sampled(st, logits, t, k, coins)
+    for a, b in zip(got1, got0):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_sampled_accept_top_p_emits_the_nucleus():
+    # 4096 copies of one root with three leaf children over a vocabulary of 16;
+    # the device's first emitted token must follow the nucleus of p(root) and
+    # never be a token outside it
+    from tree_speculative_decoding_gb300 import ddt
+    B, V, temp, top_p = 4096, 16, 0.9, 0.75
+    rng = np.random.default_rng(8)
+    l = rng.normal(scale=1.3, size=V).astype(np.float32)
+    p = np.exp((l.astype(np.float64) - l.max()) / temp)
+    p /= p.sum()
+    order = np.argsort(-l)
+    csum = np.cumsum(p[order])
+    keep = order[:int(np.searchsorted(csum, top_p)) + 1]     # distinct logits: no ties
+    q = np.zeros(V)
+    q[keep] = p[keep] / p[keep].sum()
+    assert 2 < len(keep) < V
+    T = 4
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), B)
+    kids = [int(order[0]), int(order[len(keep)]), int(order[1])]  # one outside the nucleus
+    tok = np.tile(np.array([9] + kids, np.int32), B)
+    qo = np.arange(B + 1, dtype=np.int32) * T
+    fc = np.tile(np.array([1, -1, -1, -1], np.int32), B)
+    ns = np.tile(np.array([-1, 2, 3, -1], np.int32), B)
+    logits = np.tile(l, (B * T, 1))
+    coins = rng.random((B * T, 4)).astype(np.float32)
+    d = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).to("cuda:0")  # noqa: E731
+    out = [torch.empty(B, dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty((B, 3), dtype=torch.int32, device="cuda:0"),
+           torch.empty(B, dtype=torch.int32, device="cuda:0")]
+    ddt.ddt_accept_sampled(d(tok, np.int32), d(fc, np.int32), d(ns, np.int32), d(qo, np.int32),
+                           d(logits, np.float32), d(np.full(B, temp), np.float32),
+                           d(np.zeros(B), np.int32), d(coins, np.float32), 2, *out,
+                           top_p=d(np.full(B, top_p), np.float32))
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (0, 0)
+    first = out[2][:, 0].cpu().numpy()
+    freq = np.bincount(first, minlength=V) / B
+    assert np.all(freq[q == 0] == 0)
+    assert np.abs(freq - q).max() < 4.5 * np.sqrt(0.25 / B)
 
 
 def test_sampled_accept_latches_too_few_coins():

@@ -322,7 +322,8 @@ ddt_status ddt_tree_links(const int32_t *parent, const int32_t *qo_indptr, int32
 ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_child,
                               const int32_t *next_sibling, const int32_t *qo_indptr,
                               const float *target_logits, int32_t vocab, const float *temperature,
-                              const int32_t *top_k, const float *coins, int32_t coin_stride,
+                              const int32_t *top_k, const float *top_p, const float *coins,
+                              int32_t coin_stride,
                               int32_t batch, int32_t max_depth, int32_t *accept_len,
                               int32_t *accepted_nodes, int32_t *commit_tokens, int32_t *bonus,
                               void *stream) {
@@ -335,7 +336,8 @@ ddt_status ddt_accept_sampled(const int32_t *node_token, const int32_t *first_ch
     DeviceState *st = device_state();
     if (!st) return DDT_ERR_CUDA;
     cudaError_t e = ddt::launch_accept_sampled(node_token, first_child, next_sibling, qo_indptr,
-                                               target_logits, vocab, temperature, top_k, coins,
+                                               target_logits, vocab, temperature, top_k, top_p,
+                                               coins,
                                                coin_stride, batch, max_depth, accept_len,
                                                accepted_nodes, commit_tokens, bonus, st->err,
                                                as_stream(stream));

@@ -85,7 +85,8 @@ cudaError_t launch_tree_links(const int32_t *parent, const int32_t *qo_indptr, i
 cudaError_t launch_accept_sampled(const int32_t *node_token, const int32_t *first_child,
                                   const int32_t *next_sibling, const int32_t *qo_indptr,
                                   const float *logits, int vocab, const float *temperature,
-                                  const int32_t *top_k, const float *coins, int coin_stride, int batch,
+                                  const int32_t *top_k, const float *top_p, const float *coins,
+                                  int coin_stride, int batch,
                                   int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
                                   int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
                                   cudaStream_t s);

@@ -1,16 +1,20 @@
-// ddt_sample.cu -- sampling accept: tree rejection sampling with temperature
-// and top-k, and the tree links it walks.
+// ddt_sample.cu -- sampling accept: tree rejection sampling with temperature,
+// top-k and top-p, and the tree links it walks.
 //
 // Page: "The DDTree CUDA Graph Fix: Unlocking Speculative Decoding at 109 tok/s
 // on PCIe Blackwell", section "Temperature Support: Already Working for
 // Linear, Planned for DDTree": sampling accept runs tree rejection sampling on
-// the target distribution (temperature, top-k), with the tree given as
+// the target distribution (temperature, top-k, top-p), with the tree given as
 // (retrieve_index, retrieve_next_token, retrieve_next_sibling).  The pages
 // give no algorithm text; the reading taken (target-only, deterministic
 // drafts):
 //   p(n)  = softmax(logits[n] / T) over the tokens whose logit is at least the
 //           top_k-th largest (all of them for top_k <= 0 or >= vocab, ties
 //           kept); T <= 0 means one-hot at the argmax (lowest id on ties);
+//   top-p then keeps the tokens whose logit is at least tau, the largest
+//           logit x whose mass S(x) (of p over the tokens with logit >= x)
+//           reaches top_p; tokens equal to tau are all kept and p is
+//           renormalised over the kept set (top_p outside (0, 1): no filter);
 //   at node n the children are tried in index order against the residual r
 //   (p minus the tokens already rejected): child c with token t is taken when
 //   coin[n][i] < r(t) / mass(r), else t leaves the residual;
@@ -108,11 +112,17 @@ struct SampleSmem {
     float fred[kWarps];
     int ired[kWarps];
     unsigned hist[256];
+    unsigned long long hist64[256];  // top-p: bin masses in 2^-40 units
+    unsigned long long topp_target, topp_above;
     float step[kWarps][kMaxSteps];  // mass of each 256-id step of each warp's segment
     float stepmax[kWarps][kMaxSteps];  // the step's max logit (the temperature pass)
     int removed[DDT_MAX_TOPK + 1];
     int nremoved;
-    unsigned gone[DDT_MAX_VOCAB / 32];  // the removed tokens as a bit set, for the bonus pass
+    union {
+        unsigned gone[DDT_MAX_VOCAB / 32];  // the removed tokens as a bit set, for the bonus pass
+        unsigned long long whist[kWarps][256];  // top-p radix passes: each warp's bin masses
+        unsigned whist32[kWarps][256];          // top-k radix passes: each warp's bin counts
+    };
     int decision;  // child taken, or -1
     float mass;
     int bonus;
@@ -154,13 +164,15 @@ __device__ float block_sum(float v, SampleSmem &sm) {
 __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSmem &sm) {
     unsigned prefix = 0, mask = 0;
     int need = k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0;
-        __syncthreads();
-        // equal bins within a warp are added once: after the first pass nearly all
-        // keys share their leading bits, and one shared-memory atomic per key would
-        // serialise on a handful of bins.  Eight loads in flight per thread.
-        const int lane = threadIdx.x & 31;
+        // each warp counts into a histogram of its own (atomics that only lanes of
+        // one warp contend on: after the first pass nearly all keys share their
+        // leading bits, and one histogram for the CTA would serialise all warps on
+        // a handful of bins); the warps' counts are added per bin after the pass.
+        // Eight loads in flight per thread.
+        for (int i = lane; i < 256; i += 32) sm.whist32[warp][i] = 0u;
+        __syncwarp();
         for (int v0 = threadIdx.x - lane; v0 < vocab; v0 += 8 * kThreads) {
             unsigned key[8];
 #pragma unroll
@@ -171,11 +183,15 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int v = v0 + k * kThreads + lane;
-                const bool in = v < vocab && (key[k] & mask) == prefix;
-                const unsigned bin = in ? (key[k] >> shift) & 255u : 256u;
-                const unsigned same = __match_any_sync(FULL, bin);
-                if (in && lane == __ffs(same) - 1) atomicAdd(&sm.hist[bin], (unsigned)__popc(same));
+                if (v < vocab && (key[k] & mask) == prefix)
+                    atomicAdd(&sm.whist32[warp][(key[k] >> shift) & 255u], 1u);
             }
+        }
+        __syncthreads();
+        for (int d = threadIdx.x; d < 256; d += kThreads) {
+            unsigned t = 0u;
+            for (int w = 0; w < kWarps; ++w) t += sm.whist32[w][d];
+            sm.hist[d] = t;
         }
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -196,11 +212,80 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
     return prefix;
 }
 
+// key of tau for top-p: the largest key kappa among the candidates (keys >= lo)
+// whose mass S(kappa), the sum of e^{(x - lmax)/T} over candidate keys >=
+// kappa, reaches top_p times the candidates' total.  Four 8-bit radix passes
+// over the masses in fixed point (2^-40 units: integer sums, so the decision
+// does not depend on any summation order).  Each warp adds its lanes' masses
+// into a histogram of its own (shared-memory atomics that only lanes of the
+// same warp contend on), and the warps' histograms are added per bin after
+// the pass.
+__device__ unsigned topp_key(const float *row, int vocab, unsigned lo, float lmax, float inv_t,
+                             float top_p, SampleSmem &sm) {
+    unsigned prefix = 0, mask = 0;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = lane; i < 256; i += 32) sm.whist[warp][i] = 0ull;
+        __syncwarp();
+        for (int v0 = threadIdx.x - lane; v0 < vocab; v0 += 8 * kThreads) {
+            float x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int v = v0 + k * kThreads + lane;
+                x[k] = v < vocab ? row[v] : -INFINITY;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int v = v0 + k * kThreads + lane;
+                const unsigned key = order_key(x[k]);
+                const bool in = v < vocab && key >= lo && (key & mask) == prefix;
+                if (in) {  // e <= 1 (x <= lmax), so the fixed-point mass is at most 2^40
+                    const unsigned long long f =
+                        __float2ull_rn(__expf((x[k] - lmax) * inv_t) * 1099511627776.0f);
+                    atomicAdd(&sm.whist[warp][(key >> shift) & 255u], f);
+                }
+            }
+        }
+        __syncthreads();
+        for (int d = threadIdx.x; d < 256; d += kThreads) {
+            unsigned long long t = 0ull;
+            for (int w = 0; w < kWarps; ++w) t += sm.whist[w][d];
+            sm.hist64[d] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (shift == 24) {
+                unsigned long long total = 0;
+                for (int d = 0; d < 256; ++d) total += sm.hist64[d];
+                unsigned long long target = (unsigned long long)((double)top_p * (double)total);
+                sm.topp_target = target < 1ull ? 1ull : target;
+                sm.topp_above = 0ull;
+            }
+            unsigned long long above = sm.topp_above;
+            const unsigned long long target = sm.topp_target;
+            int d = 255;
+            for (; d > 0; --d) {
+                if (above + sm.hist64[d] >= target) break;
+                above += sm.hist64[d];
+            }
+            sm.thr_key = (unsigned)d;
+            sm.topp_above = above;
+        }
+        __syncthreads();
+        prefix |= sm.thr_key << shift;
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    return prefix;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__restrict__ first_child,
                       const int32_t *__restrict__ next_sibling, const int32_t *__restrict__ qo_indptr,
                       const float *__restrict__ logits, int vocab, const float *__restrict__ temperature,
-                      const int32_t *__restrict__ top_k, const float *__restrict__ coins, int coin_stride,
+                      const int32_t *__restrict__ top_k, const float *__restrict__ top_p,
+                      const float *__restrict__ coins, int coin_stride,
                       int max_depth, int32_t *__restrict__ accept_len, int32_t *__restrict__ accepted_nodes,
                       int32_t *__restrict__ commit_tokens, int32_t *__restrict__ bonus, unsigned int *err) {
     __shared__ SampleSmem sm;
@@ -214,6 +299,9 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
     const int kk = top_k[b];
     const bool greedy = !(temp > 0.f);
     const bool use_topk = !greedy && kk > 0 && kk < vocab;
+    const float tp = top_p ? top_p[b] : 1.f;
+    const bool use_topp = !greedy && tp > 0.f && tp < 1.f;
+    const bool use_filter = use_topk || use_topp;
     const float inv_t = greedy ? 0.f : 1.f / temp;
     const int width = max_depth + 1;
     if (tid == 0 && T >= 1 && T <= DDT_MAX_Q_LEN) prefetch_row(logits + (size_t)base * vocab, vocab);
@@ -236,7 +324,7 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
     const int nsteps = s1 > s0 ? (s1 - s0 + 255) / 256 : 0;
     // at temperature > 0 without top-k the first pass also keeps, per step, the
     // sum of e^{(x - m)/T} and its max m, so the bonus draw needs no second pass
-    const bool step_pass = !greedy && !use_topk;
+    const bool step_pass = !greedy && !use_filter;
     int cur = 0, n = 1;
     if (tid == 0) path[0] = 0;
     int bon = -1;
@@ -320,8 +408,9 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
                 part += e;
             }
             z = block_sum(part, sm);
-        } else if (use_topk) {  // kept set first, then the normaliser over it
-            thr = kth_largest_key(row, vocab, kk, sm);
+        } else if (use_filter) {  // kept set first (top-k, then top-p), then the normaliser over it
+            if (use_topk) thr = kth_largest_key(row, vocab, kk, sm);
+            if (use_topp) thr = topp_key(row, vocab, thr, lmax, inv_t, tp, sm);
             float part = 0.f;
             for_each_logit(row, vocab, [&](int, float x) {
                 if (order_key(x) >= thr) part += __expf((x - lmax) * inv_t);
@@ -333,7 +422,7 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         auto prob_of = [&](int v, float x) -> float {
             if (v < 0 || v >= vocab) return 0.f;
             if (greedy) return v == amax ? 1.f : 0.f;
-            if (use_topk && order_key(x) < thr) return 0.f;
+            if (use_filter && order_key(x) < thr) return 0.f;
             return __expf((x - lmax) * inv_t) * inv_z;
         };
         // the children against the residual (one thread, shared-memory values)
@@ -424,7 +513,7 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
                     if (lane == 0) sm.step[w][st] = lsum;
                 }
             }
-        } else {  // top-k: every step per element
+        } else {  // top-k / top-p: every step per element
             for (int st = 0; st < nsteps; ++st) {
                 float loc[8], lsum;
                 int llast;
@@ -531,12 +620,14 @@ cudaError_t launch_tree_links(const int32_t *parent, const int32_t *qo_indptr, i
 cudaError_t launch_accept_sampled(const int32_t *node_token, const int32_t *first_child,
                                   const int32_t *next_sibling, const int32_t *qo_indptr,
                                   const float *logits, int vocab, const float *temperature,
-                                  const int32_t *top_k, const float *coins, int coin_stride, int batch,
+                                  const int32_t *top_k, const float *top_p, const float *coins,
+                                  int coin_stride, int batch,
                                   int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
                                   int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
                                   cudaStream_t s) {
     return launch_pdl(accept_sampled_kernel, dim3(batch), dim3(kThreads), 0, s, node_token, first_child,
-                      next_sibling, qo_indptr, logits, vocab, temperature, top_k, coins, coin_stride,
+                      next_sibling, qo_indptr, logits, vocab, temperature, top_k, top_p, coins,
+                      coin_stride,
                       max_depth, accept_len, accepted_nodes, commit_tokens, bonus, err);
 }
 

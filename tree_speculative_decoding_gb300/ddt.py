@@ -53,7 +53,8 @@ def _load():
         "ddt_accept": ([P, P, P, P, i32, i32, P, P, P, P, P], i32),
         "ddt_commit_kv": ([P, i64, P, P, P, P, P, i32, i32, P, P], i32),
         "ddt_tree_links": ([P, P, i32, P, P, P, P], i32),
-        "ddt_accept_sampled": ([P, P, P, P, P, i32, P, P, P, i32, i32, i32, P, P, P, P, P], i32),
+        "ddt_accept_sampled": ([P, P, P, P, P, i32, P, P, P, P, i32, i32, i32, P, P, P, P, P],
+                               i32),
         "ddt_get_error": ([P, P], i32),
         "ddt_selftest_wait_timeout": ([ctypes.c_uint32, P], i32),
         "ddt_verify_step": ([P, P], i32),
@@ -374,10 +375,10 @@ def ddt_tree_links(parent, qo_indptr, first_child, next_sibling, retrieve_index,
 
 def ddt_accept_sampled(node_token, first_child, next_sibling, qo_indptr, target_logits,
                        temperature, top_k, coins, max_depth, accept_len, accepted_nodes,
-                       commit_tokens, bonus, stream=None):
-    """Sampling accept: tree rejection sampling with temperature and top-k.
+                       commit_tokens, bonus, stream=None, top_p=None):
+    """Sampling accept: tree rejection sampling with temperature, top-k and top-p.
     target_logits float32 [rows, vocab]; temperature float32 [B]; top_k int32 [B];
-    coins float32 [rows, coin_stride] uniform in [0, 1)."""
+    coins float32 [rows, coin_stride] uniform in [0, 1); top_p float32 [B] or None."""
     _dev(target_logits, torch.float32, "target_logits")
     _dev(temperature, torch.float32, "temperature")
     _dev(coins, torch.float32, "coins")
@@ -387,9 +388,15 @@ def ddt_accept_sampled(node_token, first_child, next_sibling, qo_indptr, target_
                  ("commit_tokens", commit_tokens), ("bonus", bonus)):
         _dev(t, torch.int32, n)
     B = qo_indptr.numel() - 1
+    if top_p is not None:
+        _dev(top_p, torch.float32, "top_p")
+        if top_p.numel() != B:
+            raise ValueError("top_p must hold one value per request")
+    if temperature.numel() != B or top_k.numel() != B:
+        raise ValueError("temperature and top_k must hold one value per request")
     _check("ddt_accept_sampled", lib.ddt_accept_sampled(
         _p(node_token), _p(first_child), _p(next_sibling), _p(qo_indptr), _p(target_logits),
-        target_logits.shape[1], _p(temperature), _p(top_k), _p(coins), coins.shape[1], B,
+        target_logits.shape[1], _p(temperature), _p(top_k), _p(top_p), _p(coins), coins.shape[1], B,
         int(max_depth), _p(accept_len), _p(accepted_nodes), _p(commit_tokens), _p(bonus),
         _stream(stream)))
 
