@@ -78,6 +78,10 @@ constexpr int kBoxBytes = kNb * 128;  // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBytes = kNb * 64;  // 64 rows x this CTA's 32 rope dims, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBytes;  // 4 latent boxes + rope half
 constexpr int kStages = 4;
+// ring depths of the partner-partial buffers (X) and the P buffers; block j
+// uses buffer j % depth with barrier phase (j / depth) & 1
+constexpr int kXBufs = 2;
+constexpr int kPBufs = 2;
 // P (128 rows x 64 kv, bf16): one 128-byte-swizzle atom column; the 32 rows of
 // one warp are 4 contiguous KB and go to the partner as one bulk copy.
 constexpr int kPBytes = kRows * 128;
@@ -88,10 +92,10 @@ constexpr int kXBytes = (kNb / 4) * 64 * 16;
 constexpr int kOffStage = 0;
 constexpr int kORowStride = 1040;  // epilogue staging of O rows in the idle stages (16 B of padding)
 constexpr int kOffP = kOffStage + kStages * kStageBytes;  // two P buffers
-constexpr int kOffX = kOffP + 2 * kPBytes;                // two partial buffers
-constexpr int kOffQr = kOffX + 2 * kXBytes;               // Q rope half: 128 rows x 64 B, 64-byte swizzle
-constexpr int kOffAlpha = kOffQr + kRows * 64;             // 2 x 64 floats
-constexpr int kOffLinv = kOffAlpha + 2 * 64 * 4;          // 64 floats
+constexpr int kOffX = kOffP + kPBufs * kPBytes;          // partner-partial buffers
+constexpr int kOffQr = kOffX + kXBufs * kXBytes;          // Q rope half: 128 rows x 64 B, 64-byte swizzle
+constexpr int kOffAlpha = kOffQr + kRows * 64;             // 64 rescale factors per P buffer
+constexpr int kOffLinv = kOffAlpha + kPBufs * 64 * 4;     // 64 floats
 constexpr int kOffBar = kOffLinv + 64 * 4;
 // barrier slots
 enum {
@@ -99,8 +103,8 @@ enum {
     B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
     B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_ODONE, B_QLD, B_QFREE, B_COUNT
 };
-constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // 2 buffers x 2 owner warps: 4-byte "read" signals
-constexpr int kOffHolder = kOffXsig + 16;
+constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // per X buffer, 2 owner warps: 4-byte "read" signals
+constexpr int kOffHolder = kOffXsig + 8 * kXBufs;
 constexpr int kOffAbort = kOffHolder + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -129,6 +133,12 @@ constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kNb <= kTmemCols, "tensor memory budget");
 static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+static_assert(kXBufs >= 1 && kXBufs <= 2 && kPBufs >= 1 && kPBufs <= 2, "two barrier slots per ring");
+
+__device__ __forceinline__ int xbuf(int j) { return j % kXBufs; }
+__device__ __forceinline__ uint32_t xphase(int j) { return (uint32_t)(j / kXBufs) & 1u; }
+__device__ __forceinline__ int pbuf_of(int j) { return j % kPBufs; }
+__device__ __forceinline__ uint32_t pphase(int j) { return (uint32_t)(j / kPBufs) & 1u; }
 static_assert(kRows * kORowStride <= kStages * kStageBytes, "epilogue staging fits in the stages");
 
 struct TcParams {
@@ -318,7 +328,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
-    cluster_sync();  // both CTAs' barriers exist before any remote access
+    // both CTAs' barriers exist before any remote access: the inits were
+    // published by fence.mbarrier_init, so the arrive can be relaxed and the
+    // producers' kv slot loads in flight do not hold it up
+    cluster_sync_relaxed_arrive();
 
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     // Every MMA accumulates (enable-input-D set): an MMA that overwrites its
@@ -439,7 +452,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 mma_commit(bar(B_SFULL0 + (j & 1)));
             };
             auto issue_pv = [&](int k) {
-                const int s = k % kStages, pb = k & 1;
+                const int s = k % kStages, pb = pbuf_of(k);
                 tc_fence_after();
                 const uint32_t pbuf = sbase + kOffP + pb * kPBytes;
                 const uint32_t stage = sbase + kOffStage + s * kStageBytes;
@@ -463,7 +476,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     issue_s(ns++);
                     did = true;
                 }
-                if (np < ns && mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)) {
+                if (np < ns && mbar_test_wait(bar(B_PFULL0 + pbuf_of(np)), pphase(np))) {
                     issue_pv(np++);
                     did = true;
                 }
@@ -552,7 +565,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL0 + (j & 1)));
+            if (lane == 0) mbar_arrive(bar(B_PFULL0 + pbuf_of(j)));
             return true;
         };
 
@@ -571,30 +584,31 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 bool can_send = false;
                 if (nsend < nblk && nsend <= nfin + 2) {
                     bool t = mbar_test_wait(bar(B_SFULL0 + (nsend & 1)), (nsend >> 1) & 1) &&
-                             (nsend < 2 || mbar_test_wait(bar(B_XEMPTY0 + (nsend & 1)), ((nsend - 2) >> 1) & 1));
+                             (nsend < kXBufs ||
+                              mbar_test_wait(bar(B_XEMPTY0 + xbuf(nsend)), xphase(nsend - kXBufs)));
                     can_send = __shfl_sync(0xffffffffu, t, 0);
                 }
                 if (can_send) {
                     const int j = nsend++;
                     float sv[kNb];
                     take_scores(j, sv);
-                    const uint32_t dst = px_row + (j & 1) * kXBytes;
-                    const uint32_t p_xfull = map_to_cta(bar(B_XFULL0 + (j & 1)), peer);
+                    const uint32_t dst = px_row + xbuf(j) * kXBytes;
+                    const uint32_t p_xfull = map_to_cta(bar(B_XFULL0 + xbuf(j)), peer);
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q)
                         st_async_v4(dst + 64 * 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
                                     __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
                     // the owner signals "read" with a 4-byte store per owner warp
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY0 + (j & 1)), 4);
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY0 + xbuf(j)), 4);
                     did = true;
                 }
                 if (nfin < nsend) {
-                    const int s = nfin & 1;
+                    const int s = pbuf_of(nfin);
                     if (!pin_armed) {
                         if (lane == 0) mbar_arrive_expect_tx(bar(B_PIN0 + s), 32 * ((kNb / 8) * 16 + 4));
                         pin_armed = true;
                     }
-                    const bool t = __shfl_sync(0xffffffffu, mbar_test_wait(bar(B_PIN0 + s), (nfin >> 1) & 1), 0);
+                    const bool t = __shfl_sync(0xffffffffu, mbar_test_wait(bar(B_PIN0 + s), pphase(nfin)), 0);
                     if (t) {
                         const float alpha = reinterpret_cast<volatile float *>(smem + kOffAlpha)[s * 64 + xrow];
                         if (!finish_block(nfin, alpha)) { ok = false; break; }
@@ -613,9 +627,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             }
         } else {
             for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
+                const int xs = xbuf(j), s = pbuf_of(j);
                 float sv[kNb];
-                if (!wait_or_abort(bar(B_SFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                if (!wait_or_abort(bar(B_SFULL0 + (j & 1)), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
                 take_scores(j, sv);
                 const int c0 = c_begin + j * kNb;
                 const bool pre_only = all_prefix(j);
@@ -627,10 +641,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 }
                 if (j + 1 < nblk && !all_prefix(j + 1)) fetch_bits(j + 1);
                 // owner: partner partial + own partial -> softmax -> P for both CTAs
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + s), 32 * kNb * 4);
-                if (!wait_or_abort(bar(B_XFULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + xs), 32 * kNb * 4);
+                if (!wait_or_abort(bar(B_XFULL0 + xs), xphase(j), abort_flag, a.err)) { ok = false; break; }
                 {
-                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + s * kXBytes) + xrow;
+                    const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + xs * kXBytes) + xrow;
 #pragma unroll
                     for (int q = 0; q < kNb / 4; ++q) {
                         const float4 v = x[64 * q];
@@ -641,8 +655,8 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 }
                 __syncwarp();
                 if (lane == 0)
-                    st_async_b32(map_to_cta(sbase + kOffXsig + 4 * (2 * s + (warp & 1)), peer), 0u,
-                                 map_to_cta(bar(B_XEMPTY0 + s), peer));
+                    st_async_b32(map_to_cta(sbase + kOffXsig + 4 * (2 * xs + (warp & 1)), peer), 0u,
+                                 map_to_cta(bar(B_XEMPTY0 + xs), peer));
                 // visibility of the block's 64 columns: the mask bits (for a tree mask,
                 // or-ed with the prefix), and-ed with the split's range.  Rows past
                 // the tile's last valid row are never stored; their scores are finite
@@ -684,7 +698,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 }
                 l += acc.x + acc.y;
                 // both CTAs' P buffer s must be free (PV_{j-2} done in both)
-                if (j >= 2 && !wait_or_abort(bar(B_PEMPTY0 + s), ((j - 2) >> 1) & 1, abort_flag, a.err)) {
+                if (j >= kPBufs && !wait_or_abort(bar(B_PEMPTY0 + s), pphase(j - kPBufs), abort_flag, a.err)) {
                     ok = false;
                     break;
                 }

@@ -75,6 +75,13 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned; barrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
+// The same barrier with a relaxed arrive: it orders nothing by itself, so a
+// thread with loads in flight does not wait for them.  Enough to publish
+// mbarrier inits that were followed by fence.mbarrier_init.release.cluster.
+__device__ __forceinline__ void cluster_sync_relaxed_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned; barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
 // 16-byte store into another CTA's shared memory that completes `bytes` on its barrier
 __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
                                             uint32_t c, uint32_t d, uint32_t cluster_bar) {
