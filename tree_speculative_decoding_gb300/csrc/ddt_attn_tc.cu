@@ -625,6 +625,12 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     ok = false;
                 }
             }
+            // The partner's "read" signals of the last sends are the only remote
+            // writes into this CTA that nothing else waits for: take them in before
+            // teardown, so that no store of the partner's can land after this CTA
+            // has left.
+            for (int j = max(0, nsend - kXBufs); j < nsend && ok; ++j)
+                if (!warp_wait(bar(B_XEMPTY0 + xbuf(j)), xphase(j), abort_flag, a.err)) ok = false;
         } else {
             for (int j = 0; j < nblk && ok; ++j) {
                 const int xs = xbuf(j), s = pbuf_of(j);
