@@ -20,6 +20,9 @@
  *   ddt_accept_sampled      tree rejection sampling with temperature, top-k, top-p
  *   ddt_verify_step         tree + mask, attention, accept (+ commit) in one call;
  *                           ddt_step_graph_* hold the same as one CUDA graph
+ *                           (ddt_step_graph_create_io: with the step's host copies)
+ *   ddt_build_chain_visibility  a prefill chunk's chain and its causal mask
+ *   ddt_prefill_step        chain + causal mask, then the attention, in one call
  *
  * Conventions for every entry point:
  *   - Pointers marked (device) must be device memory of the current CUDA
