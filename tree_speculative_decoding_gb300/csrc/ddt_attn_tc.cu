@@ -50,8 +50,9 @@
 //     the latent boxes are staged in the second half of the stage ring and
 //     moved into tensor memory with tcgen05.cp.
 //   * The visibility mask: by default every mask bit is honoured (a block
-//     whose bits are all ones skips the per-column test; each block's words
-//     are loaded one block ahead).  When the caller states that the mask is a
+//     whose bits are all ones skips the per-column test).  A row's two words
+//     for a block are loaded one block ahead by the warp that sends the row's
+//     partial scores to the owner, and travel with them.  When the caller states that the mask is a
 //     tree mask built by this library in the same step (every prefix column
 //     visible, no column after the row's own node), prefix-only blocks read no
 //     mask word, so the attention streams the prefix while the tree build is
@@ -86,8 +87,10 @@ constexpr int kPBufs = 2;
 // one warp are 4 contiguous KB and go to the partner as one bulk copy.
 constexpr int kPBytes = kRows * 128;
 // partner partial scores: [16 chunks of 4 columns][64 rows] x 16 bytes, so one
-// warp's 16-byte stores for a chunk are 512 contiguous bytes
-constexpr int kXBytes = (kNb / 4) * 64 * 16;
+// warp's 16-byte stores for a chunk are 512 contiguous bytes; then the two mask
+// words of the block for each of the 64 rows (8 bytes per row)
+constexpr int kXScoreBytes = (kNb / 4) * 64 * 16;
+constexpr int kXBytes = kXScoreBytes + 64 * 8;
 
 constexpr int kOffStage = 0;
 constexpr int kORowStride = 1040;  // epilogue staging of O rows in the idle stages (16 B of padding)
@@ -133,6 +136,7 @@ constexpr uint32_t kIdescPV = idesc_bf16(kRows, 256, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kNb <= kTmemCols, "tensor memory budget");
 static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+static_assert(kOffQr % 512 == 0, "64-byte swizzle atom of the rope box");
 static_assert(kXBufs >= 1 && kXBufs <= 2 && kPBufs >= 1 && kPBufs <= 2, "two barrier slots per ring");
 
 __device__ __forceinline__ int xbuf(int j) { return j % kXBufs; }
@@ -507,27 +511,30 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
         const uint32_t p_linv = map_to_cta(sbase + kOffLinv + xrow * 4, peer);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        // Visibility words.  Prefix-only blocks of a library-built tree mask read
-        // none.  The mask may be the previous kernel's output: it is waited for
-        // once, before the first word is read.  A block's two words (64 columns
-        // from c0, a multiple of 64) are loaded one block ahead, so that their
-        // latency hides behind the previous block.
+        // Visibility words of a row for block j: its two words (64 columns from
+        // c0, a multiple of 64).  Prefix-only blocks of a library-built tree mask
+        // read none.  The mask may be the previous kernel's output: it is waited
+        // for once, before the first word is read.  The sender of a row's
+        // partial scores (the partner's non-owner warp) loads them one block
+        // ahead and ships them with the partials, so the owner reads them from
+        // its own shared memory.
         auto all_prefix = [&](int j) {
             const int c0 = c_begin + j * kNb;
             return a.tree_mask && c0 + kNb <= min(P, c_end);
         };
         bool mask_ready = false;
-        int nj = -1;  // the block whose words nw0 / nw1 hold
-        uint32_t nw0 = 0, nw1 = 0;
-        auto fetch_bits = [&](int j) {
+        auto mask_words = [&](int j, uint32_t &w0, uint32_t &w1) {
+            if (all_prefix(j)) {
+                w0 = w1 = 0xffffffffu;
+                return;
+            }
             if (!mask_ready) {
                 pdl_wait();
                 mask_ready = true;
             }
-            const int w0 = (c_begin + j * kNb) >> 5;
-            nw0 = (w0 < W) ? mrow[w0] : 0u;
-            nw1 = (w0 + 1 < W) ? mrow[w0 + 1] : 0u;
-            nj = j;
+            const int w = (c_begin + j * kNb) >> 5;
+            w0 = (w < W) ? mrow[w] : 0u;
+            w1 = (w + 1 < W) ? mrow[w + 1] : 0u;
         };
 
         // read S_j into registers, clear it, and hand the score buffer back to the MMA warp
@@ -574,7 +581,10 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             // they exist (two partial buffers: up to two sends ahead) and take the
             // partner's P rows (and rescale factors) as soon as they land.
             const uint32_t px_row = map_to_cta(sbase + kOffX + xrow * 16, peer);
+            const uint32_t px_mask = map_to_cta(sbase + kOffX + kXScoreBytes + xrow * 8, peer);
             int nsend = 0, nfin = 0;
+            int pj = -1;  // the block whose mask words pw0 / pw1 hold
+            uint32_t pw0 = 0u, pw1 = 0u;
             bool pin_armed = false;
             uint32_t idle = 0;
             while (nfin < nblk && ok) {
@@ -598,6 +608,19 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                     for (int q = 0; q < kNb / 4; ++q)
                         st_async_v4(dst + 64 * 16 * q, __float_as_uint(sv[4 * q]), __float_as_uint(sv[4 * q + 1]),
                                     __float_as_uint(sv[4 * q + 2]), __float_as_uint(sv[4 * q + 3]), p_xfull);
+                    // the row's mask words of block j with them, the next block's loaded now
+                    uint32_t w0, w1;
+                    if (pj == j) {
+                        w0 = pw0;
+                        w1 = pw1;
+                    } else {
+                        mask_words(j, w0, w1);
+                    }
+                    st_async_v2(px_mask + xbuf(j) * kXBytes, w0, w1, p_xfull);
+                    if (j + 1 < nblk) {
+                        mask_words(j + 1, pw0, pw1);
+                        pj = j + 1;
+                    }
                     // the owner signals "read" with a 4-byte store per owner warp
                     if (lane == 0) mbar_arrive_expect_tx(bar(B_XEMPTY0 + xbuf(j)), 4);
                     did = true;
@@ -639,16 +662,16 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 take_scores(j, sv);
                 const int c0 = c_begin + j * kNb;
                 const bool pre_only = all_prefix(j);
+                // owner: partner partial + own partial -> softmax -> P for both CTAs;
+                // the partner's partials come with this row's mask words
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + xs), 32 * (kNb * 4 + 8));
+                if (!wait_or_abort(bar(B_XFULL0 + xs), xphase(j), abort_flag, a.err)) { ok = false; break; }
                 uint32_t mw0 = 0xffffffffu, mw1 = 0xffffffffu;
                 if (!pre_only) {
-                    if (nj != j) fetch_bits(j);
-                    mw0 = nw0;
-                    mw1 = nw1;
+                    const uint2 w = reinterpret_cast<const uint2 *>(smem + kOffX + xs * kXBytes + kXScoreBytes)[xrow];
+                    mw0 = w.x;
+                    mw1 = w.y;
                 }
-                if (j + 1 < nblk && !all_prefix(j + 1)) fetch_bits(j + 1);
-                // owner: partner partial + own partial -> softmax -> P for both CTAs
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_XFULL0 + xs), 32 * kNb * 4);
-                if (!wait_or_abort(bar(B_XFULL0 + xs), xphase(j), abort_flag, a.err)) { ok = false; break; }
                 {
                     const float4 *x = reinterpret_cast<const float4 *>(smem + kOffX + xs * kXBytes) + xrow;
 #pragma unroll

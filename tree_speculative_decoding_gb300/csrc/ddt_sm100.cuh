@@ -82,6 +82,13 @@ __device__ __forceinline__ void cluster_sync_relaxed_arrive() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned; barrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
+// 8-byte store into another CTA's shared memory that completes its bytes on its barrier
+__device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+                     cluster_addr),
+                 "r"(a), "r"(b), "r"(cluster_bar)
+                 : "memory");
+}
 // 16-byte store into another CTA's shared memory that completes `bytes` on its barrier
 __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
                                             uint32_t c, uint32_t d, uint32_t cluster_bar) {
