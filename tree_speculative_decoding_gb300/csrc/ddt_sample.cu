@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include "ddt_internal.cuh"
+#include "ddt_sm100.cuh"
 
 namespace ddt {
 namespace {
@@ -69,6 +70,12 @@ tree_links_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict_
 
 // ------------------------------------------------------------- sampling accept
 constexpr int kThreads = 512;
+// A visited node's logit row of up to this many ids is copied into shared
+// memory once (one bulk copy per 32 KB), and every pass over it reads shared
+// memory instead of L2; longer rows are read from global memory.
+constexpr int kStageVocab = 45056;
+constexpr uint32_t kStageChunk = 32768;
+constexpr uint32_t kStageWaitLimit = 1u << 22;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSteps = 64;  // 256-id steps per warp segment: vocabularies up to 16 * 64 * 256
 static_assert(kWarps * kMaxSteps * 256 == DDT_MAX_VOCAB, "vocabulary bound of the ABI");
@@ -287,9 +294,12 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
                       const int32_t *__restrict__ top_k, const float *__restrict__ top_p,
                       const float *__restrict__ coins, int coin_stride,
                       int max_depth, int32_t *__restrict__ accept_len, int32_t *__restrict__ accepted_nodes,
-                      int32_t *__restrict__ commit_tokens, int32_t *__restrict__ bonus, unsigned int *err) {
+                      int32_t *__restrict__ commit_tokens, int32_t *__restrict__ bonus, int stage,
+                      unsigned int *err) {
     __shared__ SampleSmem sm;
     __shared__ int path[DDT_MAX_DEPTH + 1];
+    __shared__ __align__(8) uint64_t row_bar;
+    extern __shared__ __align__(16) float srow[];  // the staged logit row (stage != 0)
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     pdl_trigger();
@@ -326,14 +336,30 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
     // sum of e^{(x - m)/T} and its max m, so the bonus draw needs no second pass
     const bool step_pass = !greedy && !use_filter;
     int cur = 0, n = 1;
-    if (tid == 0) path[0] = 0;
+    if (tid == 0) {
+        path[0] = 0;
+        if (stage) {
+            sm100::mbar_init(sm100::smem_u32(&row_bar), 1);
+            sm100::fence_barrier_init();
+        }
+    }
     int bon = -1;
+    uint32_t visit = 0;  // staged rows so far: the parity of the row barrier
     for (;;) {
         __syncthreads();
         const float *row = logits + (size_t)(base + cur) * vocab;
         const float *u = coins + (size_t)(base + cur) * coin_stride;
         // the children of cur, from the links; then their logits and coins, in parallel
         if (tid == 0) {
+            if (stage) {  // the row into shared memory; the previous row's readers are past the barrier
+                const uint32_t bar = sm100::smem_u32(&row_bar);
+                const uint32_t bytes = (uint32_t)vocab * 4u;
+                sm100::fence_proxy_async_smem();
+                sm100::mbar_arrive_expect_tx(bar, bytes);
+                for (uint32_t off = 0; off < bytes; off += kStageChunk)
+                    sm100::bulk_load_global(sm100::smem_u32(srow) + off, reinterpret_cast<const char *>(row) + off,
+                                            min(kStageChunk, bytes - off), bar);
+            }
             int nk = 0;
             for (int c = sm.fc[cur]; c >= 0; c = sm.ns[c]) {
                 if (c <= cur || c >= T || nk >= coin_stride - 1 || nk > DDT_MAX_TOPK) {
@@ -345,6 +371,15 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
             sm.nkid = nk;
         }
         __syncthreads();
+        if (stage) {  // every thread waits for the row itself (bounded), and all agree
+            const bool got = sm100::mbar_wait(sm100::smem_u32(&row_bar), visit & 1u, kStageWaitLimit);
+            if (!__syncthreads_and(got)) {  // the copy never completed: give up on this request
+                if (tid == 0) latch(err, DDT_DEVERR_TIMEOUT);
+                return;
+            }
+            row = srow;
+            ++visit;
+        }
         const int nkid = sm.nkid;
         if (nkid < 0) {
             if (tid == 0) latch(err, DDT_DEVERR_SAMPLE);
@@ -607,6 +642,9 @@ cudaError_t sample_prepare_device() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStageVocab * (int)sizeof(float));
     return e;
 }
 
@@ -625,10 +663,13 @@ cudaError_t launch_accept_sampled(const int32_t *node_token, const int32_t *firs
                                   int max_depth, int32_t *accept_len, int32_t *accepted_nodes,
                                   int32_t *commit_tokens, int32_t *bonus, unsigned int *err,
                                   cudaStream_t s) {
-    return launch_pdl(accept_sampled_kernel, dim3(batch), dim3(kThreads), 0, s, node_token, first_child,
-                      next_sibling, qo_indptr, logits, vocab, temperature, top_k, top_p, coins,
-                      coin_stride,
-                      max_depth, accept_len, accepted_nodes, commit_tokens, bonus, err);
+    // rows that fit are staged in shared memory: whole 16-byte units at 16-byte aligned starts
+    const int stage = vocab <= kStageVocab && (vocab & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+    return launch_pdl(accept_sampled_kernel, dim3(batch), dim3(kThreads),
+                      stage ? (size_t)vocab * sizeof(float) : 0, s, node_token, first_child, next_sibling,
+                      qo_indptr, logits, vocab, temperature, top_k, top_p, coins, coin_stride, max_depth,
+                      accept_len, accepted_nodes, commit_tokens, bonus, stage, err);
 }
 
 }  // namespace ddt

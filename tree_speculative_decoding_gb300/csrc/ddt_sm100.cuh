@@ -117,6 +117,14 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, uint32_t 
 
 // bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // this CTA's shared memory to global memory, tracked as a bulk async-group
+// global -> this CTA's shared memory, completing `bytes` on the barrier (16-byte
+// aligned addresses, a multiple of 16 bytes)
+__device__ __forceinline__ void bulk_load_global(uint32_t dst_cta, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cta),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_store_global(void *dst, uint32_t src_cta, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_cta),
                  "r"(bytes)
