@@ -24,15 +24,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// arrive on a barrier of another CTA of the cluster (address from mapa)
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
-}
+// Waits acquire at CTA scope.  Every barrier a kernel here waits on is one of its
+// own CTA's; what another CTA of the cluster sends (st.async, bulk copies,
+// multicast MMA commits) lands in this CTA's shared memory and completes on
+// that barrier as a transaction, so observing the phase at CTA scope orders
+// the reads that follow.  (An acquire at cluster scope measured ~5% slower on
+// long context.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
         "selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
         : "r"(bar), "r"(parity)
@@ -45,7 +46,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
         "selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
         : "r"(bar), "r"(parity)
