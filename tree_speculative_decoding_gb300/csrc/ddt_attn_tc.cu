@@ -103,8 +103,8 @@ constexpr int kOffBar = kOffLinv + 64 * 4;
 // barrier slots
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + kStages, B_SFULL0 = B_EMPTY0 + kStages, B_SFULL1, B_SFREE0, B_SFREE1,
-    B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_PIN0, B_PIN1, B_PEMPTY0, B_PEMPTY1,
-    B_PFULL0, B_PFULL1, B_PVDONE, B_FIN, B_ODONE, B_QLD, B_QFREE, B_COUNT
+    B_XFULL0, B_XEMPTY0 = B_XFULL0 + kXBufs, B_PIN0 = B_XEMPTY0 + kXBufs, B_PEMPTY0 = B_PIN0 + kPBufs,
+    B_PFULL0 = B_PEMPTY0 + kPBufs, B_PVDONE = B_PFULL0 + kPBufs, B_FIN, B_ODONE, B_QLD, B_QFREE, B_COUNT
 };
 constexpr int kOffXsig = kOffBar + B_COUNT * 8;  // per X buffer, 2 owner warps: 4-byte "read" signals
 constexpr int kOffHolder = kOffXsig + 8 * kXBufs;
@@ -137,13 +137,14 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kNb <= kTmemCols, "tensor memory budget");
 static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 static_assert(kOffQr % 512 == 0, "64-byte swizzle atom of the rope box");
-static_assert(kXBufs >= 1 && kXBufs <= 2 && kPBufs >= 1 && kPBufs <= 2, "two barrier slots per ring");
+static_assert(kXBufs >= 1 && kXBufs <= 3 && kPBufs >= 1 && kPBufs <= 3, "ring depths");
 
 __device__ __forceinline__ int xbuf(int j) { return j % kXBufs; }
 __device__ __forceinline__ uint32_t xphase(int j) { return (uint32_t)(j / kXBufs) & 1u; }
 __device__ __forceinline__ int pbuf_of(int j) { return j % kPBufs; }
 __device__ __forceinline__ uint32_t pphase(int j) { return (uint32_t)(j / kPBufs) & 1u; }
-static_assert(kRows * kORowStride <= kStages * kStageBytes, "epilogue staging fits in the stages");
+// the epilogue stages O rows over the kv stages, P and X buffers, all idle once the last PV is done
+static_assert(kRows * kORowStride <= kOffQr - kOffStage, "epilogue staging fits before the rope of Q");
 
 struct TcParams {
     // q viewed as [total_q * num_heads rows][576] bf16: boxes of 128 rows x 64
@@ -158,7 +159,9 @@ struct TcParams {
 // handed to the producers.
 constexpr int kOffQStage = kOffStage + 2 * kStageBytes;
 constexpr uint32_t kQBytes = 4 * kRows * 128 + kRows * 64;
-static_assert(4 * kRows * 128 <= 2 * kStageBytes, "Q staging fits in two stages");
+// Q's latent boxes are staged from stage 2 on: over the later stages and the P
+// buffers, which nothing writes before Q is in tensor memory, but not the X buffers
+static_assert(kOffQStage + 4 * kRows * 128 <= kOffX, "Q staging ends before the X buffers");
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
                                               unsigned int *err) {
@@ -221,8 +224,9 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
             // commits or a TMA)
             uint32_t count = 1;
             if (i < B_EMPTY0) count = 64;                       // stage full: 64 producer lanes
-            else if (i == B_SFREE0 || i == B_SFREE1 || i == B_PFULL0 || i == B_PFULL1) count = 4;  // softmax warps
-            else if (i >= B_XFULL0 && i <= B_PEMPTY1) count = 2;  // two warps / two CTAs
+            else if (i == B_SFREE0 || i == B_SFREE1 || (i >= B_PFULL0 && i < B_PFULL0 + kPBufs))
+                count = 4;  // softmax warps
+            else if (i >= B_XFULL0 && i < B_PFULL0) count = 2;  // two warps / two CTAs
             else if (i == B_FIN) count = 2;
             mbar_init(bar(i), count);
         }
@@ -592,7 +596,7 @@ attn_tc_kernel(const __grid_constant__ TcParams prm) {
                 bool did = false;
                 // uniform readiness tests (tcgen05.ld below is warp-collective)
                 bool can_send = false;
-                if (nsend < nblk && nsend <= nfin + 2) {
+                if (nsend < nblk && nsend <= nfin + kXBufs) {
                     bool t = mbar_test_wait(bar(B_SFULL0 + (nsend & 1)), (nsend >> 1) & 1) &&
                              (nsend < kXBufs ||
                               mbar_test_wait(bar(B_XEMPTY0 + xbuf(nsend)), xphase(nsend - kXBufs)));
