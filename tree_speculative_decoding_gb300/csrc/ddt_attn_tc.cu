@@ -27,7 +27,7 @@
 //     pair swaps fp32 partials through distributed shared memory: CTA c owns
 //     the softmax of rows [64c, 64c+64).  The owner adds the two partials,
 //     applies the mask, runs the online softmax (the running max moves only
-//     when a block max exceeds it by more than 2^48), writes P (bf16) locally
+//     when a block max exceeds it by more than a factor 2^48), writes P (bf16) locally
 //     and bulk-copies its rows to the partner with the rows' rescale factors.
 //     Each CTA then accumulates O_c += P V_c (tcgen05.mma, M=128, N=256, K=64,
 //     V read as an MN-major operand straight from the gathered stage).  P and
@@ -47,16 +47,17 @@
 //   * Q: the tile's rows are one contiguous block of q, so the MMA warp loads
 //     this CTA's half with TMA tensor tiles as soon as the request's offsets
 //     are known: the rope box lands in its 64-byte-swizzled operand layout,
-//     the latent boxes are staged in the second half of the stage ring and
-//     moved into tensor memory with tcgen05.cp.
+//     the latent boxes are staged from the third kv stage on and moved into
+//     tensor memory with tcgen05.cp.
 //   * The visibility mask: by default every mask bit is honoured (a block
 //     whose bits are all ones skips the per-column test).  A row's two words
 //     for a block are loaded one block ahead by the warp that sends the row's
-//     partial scores to the owner, and travel with them.  When the caller states that the mask is a
-//     tree mask built by this library in the same step (every prefix column
-//     visible, no column after the row's own node), prefix-only blocks read no
-//     mask word, so the attention streams the prefix while the tree build is
-//     still running, and columns after the tile's last node are skipped.
+//     partial scores to the owner, and travel with them.  When the caller
+//     states that the mask is a tree mask built by this library in the same
+//     step (every prefix column visible, no column after the row's own node),
+//     prefix-only blocks read no mask word, so the attention streams the prefix
+//     while the tree build is still running, and columns after the tile's last
+//     node are skipped.
 //   * Every wait is bounded; on timeout the CTA latches DDT_DEVERR_TIMEOUT,
 //     stops, and still meets its partner at the final cluster barrier.
 #include <cuda_runtime.h>
