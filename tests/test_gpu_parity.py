@@ -570,6 +570,83 @@ def test_verify_attn_honours_every_mask_bit(splits):
     assert not np.allclose(got, st.out.reshape(-1, 512).double().cpu().numpy())
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+def test_verify_attn_takes_a_random_mask(splits):
+    # every bit of a ragged batch's mask drawn at random (70% set), so that almost
+    # every 64-column block, prefix blocks included, takes the per-column select;
+    # every row against the oracle, which honours every bit
+    from tree_speculative_decoding_gb300 import ddt
+    wl = workloads.make_workload("random_mask", 919, 3, 8, [300, 17, 129], [40, 127, 5], 8, 4000, 2.0)
+    st = _step(wl, num_splits=splits)
+    rng = np.random.default_rng(919)
+    mask = np.zeros(int(st.mask_indptr_host[-1]), np.uint32)
+    for b in range(wl.B):
+        T, N = int(wl.q_len[b]), int(wl.kv_len[b])
+        W = (N + 31) // 32
+        bits = rng.random((T, W * 32)) < 0.7
+        bits[:, N:] = False                       # padding bits stay zero
+        words = np.packbits(bits.astype(np.uint8), axis=1, bitorder="little").view("<u4")
+        m0 = int(st.mask_indptr_host[b])
+        mask[m0:m0 + T * W] = words.reshape(-1)
+    dmask = torch.from_numpy(mask.view(np.int32)).to("cuda:0")
+    out = torch.full_like(st.out, float("nan"))
+    lse = torch.full_like(st.lse, float("nan"))
+    ddt.ddt_verify_attn(st.q, st.kv_pool, st.kv_indices, st.kv_indptr, st.qo_indptr, dmask,
+                        st.mask_indptr, wl.scale, out, lse, max_q_len=st.max_q_len,
+                        max_kv_len=st.max_kv_len, num_splits=splits, workspace=st.workspace)
+    torch.cuda.synchronize()
+    assert ddt.ddt_get_error() == (0, 0)
+    assert st.launched_splits == splits
+    ref, ref_lse = oracle.verify_attn(wl.q, wl.kv_pool, wl.kv_indices, wl.kv_indptr,
+                                      wl.qo_indptr, mask, st.mask_indptr_host.numpy(), wl.H, wl.scale)
+    got = out.reshape(-1, 512).double().cpu().numpy()
+    diff = np.abs(got - ref)
+    assert diff.max() <= MAX_TOL * np.abs(ref).max()
+    assert diff.sum() / np.abs(ref).sum() <= MEAN_TOL
+    np.testing.assert_allclose(lse.reshape(-1).double().cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-3)
+
+
+def test_prefill_chunk_with_forced_splits():
+    # ddt_prefill_step through the split path (partials + combine), every row
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.make_workload("prefill_split", 4290, 2, 8, [700, 250], [127, 90], 8, 4000, 1.0)
+    st = VerifyStep(wl, "cuda:0", num_splits=3)
+    assert st.launched_splits == 3
+    st.run_prefill()
+    torch.cuda.synchronize()
+    st.check_device_errors()
+    par = np.concatenate([np.arange(-1, T - 1) for T in wl.q_len]).astype(np.int32)
+    mask, mip = oracle.compile_visibility(par, wl.qo_indptr, wl.prefix_len)
+    assert np.array_equal(st.mask.cpu().numpy().view(np.uint32), mask)
+    _check_attn(st, wl, mask, mip, _sample_rows(wl, 10 ** 9))
+
+
+def test_step_graph_with_host_copies_and_commit():
+    # the host-copy graph with the KV commit: the results in host memory and the
+    # pool on the device equal the staged calls'
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.preset("tiny_p21_b8_h8")
+    am = _chain_forcing(wl)
+    st = _step(wl, argmax=am)
+    st.commit_kv()
+    torch.cuda.synchronize()
+    st2 = VerifyStep(wl, "cuda:0", target_argmax=am)
+    h_in = st2.inputs.buf.cpu().pin_memory()
+    h_out = torch.zeros_like(st2.outputs.buf, device="cpu").pin_memory()
+    g = st2.step_graph(commit_kv=True, host_io=(h_in, h_out))
+    g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    assert torch.equal(st.kv_pool, st2.kv_pool)
+    for name in ("accept_len", "accepted_nodes", "commit_tokens", "bonus", "new_len"):
+        v = st2.outputs.views[name]
+        off = v.data_ptr() - st2.outputs.buf.data_ptr()
+        got = h_out[off:off + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+        assert torch.equal(got, getattr(st, name).cpu()), name
+    assert st.accept_len.max().item() > 1
+    g.close()
+
+
 def test_inconsistent_offsets_are_latched_and_nothing_is_written():
     # qo_indptr past total_q, a negative qo_indptr and a negative mask_indptr,
     # each made on the host: the attention latches the bit and writes no row
