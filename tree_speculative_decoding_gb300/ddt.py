@@ -160,6 +160,10 @@ def ddt_build_chain_visibility(qo_indptr, prefix_len, mask_indptr, parent, depth
     if not (mask.is_cuda and mask.dtype in (torch.int32, torch.uint32) and mask.is_contiguous()):
         raise ValueError("mask must be a contiguous CUDA 32-bit tensor")
     B = prefix_len.numel()
+    if qo_indptr.numel() != B + 1 or mask_indptr.numel() != B + 1:
+        raise ValueError("qo_indptr and mask_indptr must hold batch + 1 offsets")
+    if parent.numel() != depth.numel():
+        raise ValueError("parent and depth must have the same length")
     _check("ddt_build_chain_visibility", lib.ddt_build_chain_visibility(
         _p(qo_indptr), _p(prefix_len), _p(mask_indptr), B, _p(parent), _p(depth), _p(mask),
         _stream(stream)))
