@@ -82,3 +82,15 @@ def test_gpus_n_without_torchrun_starts_n_ranks():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_replica_count_covers_l2():
+    import bench
+    # copies whose step inputs together cover three L2s, clamped to [2, 64]
+    l2 = 126 * 2 ** 20
+    for per in (7.3e6, 30e6, 151e6, 1e9):
+        n = bench.replica_count(per, l2)
+        assert 2 <= n <= 64
+        if n < 64:
+            assert n * per >= 3 * l2 and (n == 2 or (n - 1) * per < 3 * l2)
+    assert bench.replica_count(1, l2) == 64 and bench.replica_count(1e12, l2) == 2
