@@ -317,6 +317,31 @@ def test_step_graph_with_host_copies_returns_the_step_in_host_memory():
         st2.step_graph(host_io=(st2.inputs.buf.cpu(), h_out))
 
 
+def test_step_graph_returns_only_the_accept_results_when_asked():
+    # a host buffer of results_bytes takes the accept results alone (they lead the
+    # output buffer); the attention output stays on the device
+    from tree_speculative_decoding_gb300.pipeline import VerifyStep
+    wl = workloads.preset("ragged_bs8_b32_h64")
+    st, _ = _full_check(wl, n_rows=64)
+    st2 = VerifyStep(wl, "cuda:0")
+    assert st2.results_bytes == st2.outputs.offsets["out"] < st2.outputs.buf.numel()
+    h_in = st2.inputs.buf.cpu().pin_memory()
+    h_res = torch.full((st2.results_bytes,), 0x5A, dtype=torch.uint8).pin_memory()
+    st2.inputs.buf.zero_()
+    g = st2.step_graph(host_io=(h_in, h_res))
+    g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    for name in ("accept_len", "accepted_nodes", "commit_tokens", "bonus"):
+        v = st2.outputs.views[name]
+        off = v.data_ptr() - st2.outputs.buf.data_ptr()
+        assert off + v.numel() * v.element_size() <= st2.results_bytes
+        got = h_res[off:off + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+        assert torch.equal(got, getattr(st, name).cpu()), name
+    assert torch.equal(st2.out, st.out)            # computed on the device all the same
+    g.close()
+
+
 def test_step_graph_reports_a_host_check_and_makes_no_graph():
     from tree_speculative_decoding_gb300 import ddt
     from tree_speculative_decoding_gb300.pipeline import VerifyStep

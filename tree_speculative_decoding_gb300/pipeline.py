@@ -39,6 +39,7 @@ class _Arena:
             layout.append((name, dtype, shape, off, nbytes, None if isinstance(src, tuple) else src))
             off += (nbytes + 255) // 256 * 256
         self.buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.offsets = {name: o for name, _, _, o, _, _ in layout}
         self.views = {}
         for name, dtype, shape, o, nbytes, src in layout:
             v = self.buf[o:o + nbytes].view(dtype).view(shape)
@@ -81,13 +82,17 @@ class VerifyStep:
             ("q", torch.bfloat16, wl.q)], dev)
         for name, t in self.inputs.views.items():
             setattr(self, name, t)
+        # The accept results come first: they are what a host reads back every
+        # step (results_bytes from the start of the buffer); the attention output
+        # and its lse follow, for a caller that wants them on the host too.
         self.outputs = _Arena([
-            ("out", torch.float32, (T, self.H, ddt.DL)), ("lse", torch.float32, (T, self.H)),
             ("accept_len", torch.int32, (self.B,)), ("accepted_nodes", torch.int32, (self.B, W)),
             ("commit_tokens", torch.int32, (self.B, W)), ("bonus", torch.int32, (self.B,)),
-            ("new_len", torch.int32, (self.B,))], dev)
+            ("new_len", torch.int32, (self.B,)),
+            ("out", torch.float32, (T, self.H, ddt.DL)), ("lse", torch.float32, (T, self.H))], dev)
         for name, t in self.outputs.views.items():
             setattr(self, name, t)
+        self.results_bytes = self.outputs.offsets["out"]
         self.kv_pool = _bf16(wl.kv_pool, dev)  # the resident cache, not a per-step input
         self.node_token = torch.empty(T, dtype=torch.int32, device=dev)
         self.parent = torch.empty(T, dtype=torch.int32, device=dev)
@@ -178,9 +183,11 @@ class VerifyStep:
 
     def step_graph(self, commit_kv=False, host_io=None):
         """A library-owned CUDA graph of the step (ddt_step_graph_*).  host_io =
-        (h_in, h_out), pinned host buffers the size of the input and output
-        arenas: the graph then copies h_in into the inputs before the step and
-        the outputs into h_out after it (ddt_step_graph_create_io)."""
+        (h_in, h_out), pinned host buffers: the graph then copies h_in into the
+        inputs before the step and the first len(h_out) bytes of the outputs
+        into h_out after it (ddt_step_graph_create_io).  h_out of results_bytes
+        brings back the accept results alone; of the whole output buffer, the
+        attention output and lse as well."""
         io = None
         if host_io is not None:
             io = (host_io[0], self.inputs.buf, host_io[1], self.outputs.buf)
