@@ -338,6 +338,7 @@ def run_device(args, rank, world, local_rank):
     commit_ms = time_commit(st, stream, flush)
     sampled_ms = time_sampled(st, stream, flush, wl.vocab)
     sampled_topp_ms = time_sampled(st, stream, flush, wl.vocab, top_p=0.9)
+    sampled_topk_ms = time_sampled(st, stream, flush, wl.vocab, top_k=20)
     degenerate = time_degenerate(dev, stream, flush)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     ms_per_step = elapsed_max * 1e3 / args.steps
@@ -390,8 +391,9 @@ def run_device(args, rank, world, local_rank):
                     "call": "the same graph also copying the fp32 attention output and lse back"}},
         "gpu_launches": launches_per_step * args.steps,
         "accept_sampled": {"ms": round(sampled_ms, 5), "top_p_0.9_ms": round(sampled_topp_ms, 5),
+                           "top_k_20_ms": round(sampled_topk_ms, 5),
                            "timing": "ddt_tree_links + "
-                           "ddt_accept_sampled after the step (temperature 1, no top-k, vocab "
+                           "ddt_accept_sampled after the step (temperature 1, no top-k or top-p unless named, vocab "
                            f"{wl.vocab}, seeded N(0,1.5) logits); graph replay, L2 flushed, median"},
         "commit_kv": {"ms": round(commit_ms, 5), "timing": "ddt_commit_kv alone after the step, each "
                       "request committing its deepest root-to-leaf path; graph replay, L2 flushed, "
@@ -458,10 +460,10 @@ def time_commit(st, stream, flush, reps=200):
     return ms
 
 
-def time_sampled(st, stream, flush, vocab, reps=200, top_p=None):
+def time_sampled(st, stream, flush, vocab, reps=200, top_p=None, top_k=0):
     """Median time of the sampling accept (links + rejection sampling) on the
-    step's tree with seeded target logits, temperature 1, no top-k, and top-p
-    `top_p` (None: no top-p)."""
+    step's tree with seeded target logits, temperature 1, top-k `top_k` (0:
+    none) and top-p `top_p` (None: none)."""
     import torch
     from tree_speculative_decoding_gb300 import ddt
     dev = st.node_token.device
@@ -471,14 +473,14 @@ def time_sampled(st, stream, flush, vocab, reps=200, top_p=None):
     logits = torch.randn((rows, vocab), generator=gen, device=dev) * 1.5
     coins = torch.rand((rows, st.wl.K + 1), generator=gen, device=dev)
     temp = torch.ones(st.B, dtype=torch.float32, device=dev)
-    top_k = torch.zeros(st.B, dtype=torch.int32, device=dev)
+    tk = torch.full((st.B,), top_k, dtype=torch.int32, device=dev)
     tp = None if top_p is None else torch.full((st.B,), top_p, dtype=torch.float32, device=dev)
     fc, ns, ri = (torch.empty(rows, dtype=torch.int32, device=dev) for _ in range(3))
     out = [torch.empty_like(t) for t in (st.accept_len, st.accepted_nodes, st.commit_tokens, st.bonus)]
 
     def body(s):
         ddt.ddt_tree_links(st.parent, st.qo_indptr, fc, ns, ri, stream=s)
-        ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, logits, temp, top_k, coins,
+        ddt.ddt_accept_sampled(st.node_token, fc, ns, st.qo_indptr, logits, temp, tk, coins,
                                st.wl.max_depth, *out, stream=s, top_p=tp)
     with torch.cuda.stream(stream):
         body(stream)

@@ -128,6 +128,9 @@ struct SampleSmem {
     union {
         unsigned gone[DDT_MAX_VOCAB / 32];  // the removed tokens as a bit set, for the bonus pass
         unsigned long long whist[kWarps][256];  // top-p radix passes: each warp's bin masses
+        struct {  // the same as two 32-bit halves (rows of at most kStageVocab ids)
+            unsigned hi[kWarps][256], lo[kWarps][256];
+        } wsplit;
         unsigned whist32[kWarps][256];          // top-k radix passes: each warp's bin counts
     };
     int decision;  // child taken, or -1
@@ -226,14 +229,24 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
 // does not depend on any summation order).  Each warp adds its lanes' masses
 // into a histogram of its own (shared-memory atomics that only lanes of the
 // same warp contend on), and the warps' histograms are added per bin after
-// the pass.
+// the pass.  For rows of at most kStageVocab ids a warp adds at most 2816
+// masses per bin, so each mass (at most 2^40) goes in as two 32-bit halves,
+// bits 20 and up and the low 20 bits, whose per-warp sums stay below 2^32: two
+// native 32-bit shared atomics instead of one 64-bit one.
 __device__ unsigned topp_key(const float *row, int vocab, unsigned lo, float lmax, float inv_t,
                              float top_p, SampleSmem &sm) {
+    static_assert(((kStageVocab + kThreads - 1) / kThreads) * 32 * (1ull << 20) < (1ull << 32),
+                  "per-warp sums of the 32-bit halves fit");
     unsigned prefix = 0, mask = 0;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const bool halves = vocab <= kStageVocab;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = lane; i < 256; i += 32) sm.whist[warp][i] = 0ull;
+        if (halves) {
+            for (int i = lane; i < 256; i += 32) sm.wsplit.hi[warp][i] = sm.wsplit.lo[warp][i] = 0u;
+        } else {
+            for (int i = lane; i < 256; i += 32) sm.whist[warp][i] = 0ull;
+        }
         __syncwarp();
         for (int v0 = threadIdx.x - lane; v0 < vocab; v0 += 8 * kThreads) {
             float x[8];
@@ -250,34 +263,69 @@ __device__ unsigned topp_key(const float *row, int vocab, unsigned lo, float lma
                 if (in) {  // e <= 1 (x <= lmax), so the fixed-point mass is at most 2^40
                     const unsigned long long f =
                         __float2ull_rn(__expf((x[k] - lmax) * inv_t) * 1099511627776.0f);
-                    atomicAdd(&sm.whist[warp][(key >> shift) & 255u], f);
+                    const unsigned b = (key >> shift) & 255u;
+                    if (halves) {
+                        atomicAdd(&sm.wsplit.hi[warp][b], (unsigned)(f >> 20));
+                        atomicAdd(&sm.wsplit.lo[warp][b], (unsigned)(f & 0xFFFFFull));
+                    } else {
+                        atomicAdd(&sm.whist[warp][b], f);
+                    }
                 }
             }
         }
         __syncthreads();
         for (int d = threadIdx.x; d < 256; d += kThreads) {
             unsigned long long t = 0ull;
-            for (int w = 0; w < kWarps; ++w) t += sm.whist[w][d];
+            if (halves) {
+                for (int w = 0; w < kWarps; ++w)
+                    t += ((unsigned long long)sm.wsplit.hi[w][d] << 20) + sm.wsplit.lo[w][d];
+            } else {
+                for (int w = 0; w < kWarps; ++w) t += sm.whist[w][d];
+            }
             sm.hist64[d] = t;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        // Warp 0 walks the bins from the top (d = 255 down to 1) to the first whose
+        // mass, added to the mass above it, reaches the target; bin 0 if none does.
+        // Lane l holds bins 255 - 8l .. 248 - 8l; a prefix sum over the lanes finds
+        // the lane where the running mass crosses, which then walks its eight bins.
+        if (warp == 0) {
+            unsigned long long h[8], part = 0ull;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = sm.hist64[255 - 8 * lane - i];
+                part += h[i];
+            }
+            unsigned long long incl = part;  // bins of lanes 0..lane
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long t = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += t;
+            }
+            unsigned long long above = sm.topp_above, target = sm.topp_target;
             if (shift == 24) {
-                unsigned long long total = 0;
-                for (int d = 0; d < 256; ++d) total += sm.hist64[d];
-                unsigned long long target = (unsigned long long)((double)top_p * (double)total);
-                sm.topp_target = target < 1ull ? 1ull : target;
-                sm.topp_above = 0ull;
+                const unsigned long long total = __shfl_sync(FULL, incl, 31);
+                target = (unsigned long long)((double)top_p * (double)total);
+                target = target < 1ull ? 1ull : target;
+                above = 0ull;
             }
-            unsigned long long above = sm.topp_above;
-            const unsigned long long target = sm.topp_target;
-            int d = 255;
-            for (; d > 0; --d) {
-                if (above + sm.hist64[d] >= target) break;
-                above += sm.hist64[d];
+            const unsigned cross = __ballot_sync(FULL, above + incl >= target);
+            const int cl = cross ? __ffs(cross) - 1 : 31;
+            if (lane == cl) {
+                unsigned long long run = above + (incl - part);
+                int d = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int di = 255 - 8 * lane - i;
+                    if (d == 0 && di > 0) {
+                        if (run + h[i] >= target) d = di;
+                        else run += h[i];
+                    }
+                }
+                sm.thr_key = (unsigned)d;
+                sm.topp_above = run;
+                sm.topp_target = target;
             }
-            sm.thr_key = (unsigned)d;
-            sm.topp_above = above;
         }
         __syncthreads();
         prefix |= sm.thr_key << shift;
@@ -443,13 +491,26 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
                 part += e;
             }
             z = block_sum(part, sm);
-        } else if (use_filter) {  // kept set first (top-k, then top-p), then the normaliser over it
+        } else if (use_filter) {  // kept set first (top-k, then top-p), then its mass per step
             if (use_topk) thr = kth_largest_key(row, vocab, kk, sm);
             if (use_topp) thr = topp_key(row, vocab, thr, lmax, inv_t, tp, sm);
+            // the kept mass of each 256-id step of this warp's segment, as the
+            // temperature pass keeps it, so that the bonus draw recomputes only
+            // the steps of removed tokens; z is the total
             float part = 0.f;
-            for_each_logit(row, vocab, [&](int, float x) {
-                if (order_key(x) >= thr) part += __expf((x - lmax) * inv_t);
-            });
+            for (int st = 0; st < nsteps; ++st) {
+                const int b0 = s0 + 256 * st + 8 * lane;
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[k] = b0 + k < s1 ? row[b0 + k] : -INFINITY;
+                float e = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (b0 + k < s1 && order_key(x[k]) >= thr) e += __expf((x[k] - lmax) * inv_t);
+                part += e;
+                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(FULL, e, o);
+                if (lane == 0) sm.step[warp][st] = e;
+            }
             z = block_sum(part, sm);
         }
         // p(v) of the target at this node (0 outside the kept set), from its logit
@@ -495,8 +556,7 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         const int nrem = sm.nremoved;
         const float target = u[coin_stride - 1] * sm.mass;
         for (int i = tid; i < (vocab + 31) >> 5; i += kThreads) sm.gone[i] = 0u;
-        if (step_pass)  // step masses as probabilities
-            for (int st = lane; st < nsteps; st += 32) sm.step[warp][st] *= inv_z;
+        for (int st = lane; st < nsteps; st += 32) sm.step[warp][st] *= inv_z;  // step masses as probabilities
         __syncthreads();
         if (tid < nrem) {
             const int t = sm.removed[tid];
@@ -528,33 +588,24 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
             for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(FULL, lsum, o);
             return lsum;
         };
-        if (step_pass) {
-            // only the steps holding a removed token change: warp j recomputes the
-            // step of removed token j per element, once per step (steps are the
-            // id blocks [256i, 256i + 256), since seg is a multiple of 256)
-            for (int j = warp; j < nrem; j += kWarps) {
-                const int t = sm.removed[j];
-                bool first = t >= 0 && t < vocab;
-                for (int r = 0; r < j && first; ++r) {
-                    const int q = sm.removed[r];
-                    if (q >= 0 && q < vocab && q >> 8 == t >> 8) first = false;
-                }
-                if (first) {
-                    const int w = t / seg, st = (t - w * seg) >> 8;
-                    float loc[8], lsum;
-                    int llast;
-                    step_sums(w, st, loc, lsum, llast);
-                    lsum = warp_total(lsum);
-                    if (lane == 0) sm.step[w][st] = lsum;
-                }
+        // only the steps holding a removed token change (every step's mass is known
+        // from the temperature pass or the kept-set pass): warp j recomputes the
+        // step of removed token j per element, once per step (steps are the
+        // id blocks [256i, 256i + 256), since seg is a multiple of 256)
+        for (int j = warp; j < nrem; j += kWarps) {
+            const int t = sm.removed[j];
+            bool first = t >= 0 && t < vocab;
+            for (int r = 0; r < j && first; ++r) {
+                const int q = sm.removed[r];
+                if (q >= 0 && q < vocab && q >> 8 == t >> 8) first = false;
             }
-        } else {  // top-k / top-p: every step per element
-            for (int st = 0; st < nsteps; ++st) {
+            if (first) {
+                const int w = t / seg, st = (t - w * seg) >> 8;
                 float loc[8], lsum;
                 int llast;
-                step_sums(warp, st, loc, lsum, llast);
+                step_sums(w, st, loc, lsum, llast);
                 lsum = warp_total(lsum);
-                if (lane == 0) sm.step[warp][st] = lsum;
+                if (lane == 0) sm.step[w][st] = lsum;
             }
         }
         __syncthreads();
