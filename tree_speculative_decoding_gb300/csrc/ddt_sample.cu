@@ -204,14 +204,38 @@ __device__ unsigned kth_largest_key(const float *row, int vocab, int k, SampleSm
             sm.hist[d] = t;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int above = 0, d = 255;
-            for (; d > 0; --d) {
-                if (above + (int)sm.hist[d] >= need) break;
-                above += (int)sm.hist[d];
+        // Warp 0 walks the bins from the top (d = 255 down to 1) to the first whose
+        // count, added to the count above it, reaches the rank; bin 0 if none does
+        // (lane l holds bins 255 - 8l .. 248 - 8l, as in topp_key).
+        if (warp == 0) {
+            unsigned h[8], part = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = sm.hist[255 - 8 * lane - i];
+                part += h[i];
             }
-            sm.thr_key = (unsigned)d;
-            sm.nremoved = need - above;  // reused as scratch: rank inside the bin
+            unsigned incl = part;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned t = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const unsigned cross = __ballot_sync(FULL, incl >= (unsigned)need);
+            const int cl = cross ? __ffs(cross) - 1 : 31;
+            if (lane == cl) {
+                unsigned above = incl - part;
+                int d = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int di = 255 - 8 * lane - i;
+                    if (d == 0 && di > 0) {
+                        if (above + h[i] >= (unsigned)need) d = di;
+                        else above += h[i];
+                    }
+                }
+                sm.thr_key = (unsigned)d;
+                sm.nremoved = need - (int)above;  // reused as scratch: rank inside the bin
+            }
         }
         __syncthreads();
         prefix |= sm.thr_key << shift;
