@@ -896,7 +896,10 @@ int attn_choose_splits(int batch, int num_heads, int max_q_len, int max_kv_len, 
     const long long pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
     if (batch > 1 && tiles >= pairs) return 1;
     const long long blocks = ((long long)max_kv_len + kNb - 1) / kNb;
-    long long smax = blocks / 4;  // keep >= 4 blocks per split
+    // every split keeps >= 4 blocks as launched (ceil(blocks / s) >= 4): the launch
+    // gives each split a whole number of blocks, so a cap of blocks / 4 would leave
+    // 4.x-block counts that round up to 5
+    long long smax = blocks >= 4 ? (blocks - 1) / 3 : 1;
     if (smax > DDT_MAX_SPLITS) smax = DDT_MAX_SPLITS;
     if (smax > max_splits) smax = max_splits;
     if (smax < 1) smax = 1;
