@@ -637,32 +637,67 @@ accept_sampled_kernel(const int32_t *__restrict__ node_token, const int32_t *__r
         // order (the same numbers in every lane), or, if rounding left the target
         // above the total, the last step with mass; then that step per element
         if (warp == 0) {
-            float pre = 0.f, cpre = 0.f, lpre = 0.f;
-            int cw = -1, cs = -1, lw = -1, ls = -1;
-            for (int w = 0; w < kWarps && cw < 0; ++w) {
+            // Step g in id order is step g % nsw of warp g / nsw's segment (nsw = seg /
+            // 256 steps each; the last segments hold fewer or none).  Lane l sums the
+            // steps [c l, c l + c); a prefix sum over the lanes finds the lane where
+            // the running mass passes the target, and that lane walks its steps.
+            const int nsw = seg >> 8;
+            const int nst = kWarps * nsw;
+            const int c = (nst + 31) >> 5;
+            auto step_mass = [&](int g) -> float {
+                if (g >= nst) return 0.f;
+                const int w = g / nsw, st = g - w * nsw;
                 const int ws0 = w * seg, ws1 = min(vocab, ws0 + seg);
                 const int wn = ws1 > ws0 ? (ws1 - ws0 + 255) / 256 : 0;
-                for (int st = 0; st < wn; ++st) {
-                    const float mass_s = sm.step[w][st];
-                    const float nxt = pre + mass_s;
-                    if (pre <= target && target < nxt) {
-                        cw = w;
-                        cs = st;
-                        cpre = pre;
-                        break;
-                    }
-                    if (mass_s > 0.f) {
-                        lw = w;
-                        ls = st;
-                        lpre = pre;
-                    }
-                    pre = nxt;
-                }
+                return st < wn ? sm.step[w][st] : 0.f;
+            };
+            float part = 0.f;
+            for (int i = 0; i < c; ++i) part += step_mass(lane * c + i);
+            float incl = part;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += y;
             }
-            if (cw < 0) {
-                cw = lw;
-                cs = ls;
-                cpre = lpre;
+            float excl = __shfl_up_sync(FULL, incl, 1);
+            if (lane == 0) excl = 0.f;
+            // the lane to walk: the crossing one, or, if rounding left the target at
+            // or above the total, the last lane with mass (then its last step with mass)
+            const unsigned over = __ballot_sync(FULL, target < incl);
+            const unsigned has = __ballot_sync(FULL, part > 0.f);
+            const int wl = over ? __ffs(over) - 1 : (has ? 31 - __clz(has) : -1);
+            int cw = -1, cs = -1;
+            float cpre = 0.f;
+            if (wl >= 0) {
+                if (lane == wl) {
+                    float pre = excl;
+                    int fw = -1, fs = -1;
+                    float fpre = 0.f;
+                    for (int i = 0; i < c; ++i) {
+                        const int g = lane * c + i;
+                        const float m = step_mass(g);
+                        if (over && pre <= target && target < pre + m) {
+                            cw = g / nsw;
+                            cs = g - cw * nsw;
+                            cpre = pre;
+                            break;
+                        }
+                        if (m > 0.f) {
+                            fw = g / nsw;
+                            fs = g - fw * nsw;
+                            fpre = pre;
+                        }
+                        pre += m;
+                    }
+                    if (cw < 0) {  // rounding: the lane's last step with mass
+                        cw = fw;
+                        cs = fs;
+                        cpre = fpre;
+                    }
+                }
+                cw = __shfl_sync(FULL, cw, wl);
+                cs = __shfl_sync(FULL, cs, wl);
+                cpre = __shfl_sync(FULL, cpre, wl);
             }
             int pick = amax;  // no residual mass at all
             if (cw >= 0) {
