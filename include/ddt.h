@@ -559,8 +559,12 @@ ddt_status ddt_step_graph_create(const ddt_step_args *args, ddt_step_graph **gra
  * pinned host memory (cudaHostAlloc or registered), d_in and d_out device
  * memory that the caller lays out so that the step's inputs and results fall
  * inside them (one packed buffer each way); all four stay allocated for the
- * graph's life.  A size of 0 omits that copy.  Returns DDT_ERR_INVALID_ARG
- * for a null or unpinned host buffer, else as ddt_step_graph_create.
+ * graph's life.  A size of 0 omits that copy.  Where a host buffer has a device
+ * pointer (cudaHostGetDevicePointer), both addresses are 16-byte aligned and the
+ * size is whole 16-byte units, the copy is a kernel reading or writing the host
+ * memory through that pointer; otherwise it is a copy-engine transfer.  Returns
+ * DDT_ERR_INVALID_ARG for a null or unpinned host buffer, else as
+ * ddt_step_graph_create.
  */
 ddt_status ddt_step_graph_create_io(const ddt_step_args *args, const void *h_in, void *d_in,
                                     size_t in_bytes, void *h_out, const void *d_out,

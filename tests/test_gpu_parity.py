@@ -340,6 +340,14 @@ def test_step_graph_returns_only_the_accept_results_when_asked():
         assert torch.equal(got, getattr(st, name).cpu()), name
     assert torch.equal(st2.out, st.out)            # computed on the device all the same
     g.close()
+    # a host buffer that is not whole 16-byte units takes the copy-engine path
+    h_odd = torch.full((st2.results_bytes - 4,), 0x5A, dtype=torch.uint8).pin_memory()
+    g = st2.step_graph(host_io=(h_in, h_odd))
+    g.launch()
+    torch.cuda.synchronize()
+    st2.check_device_errors()
+    assert torch.equal(h_odd, h_res[:st2.results_bytes - 4])
+    g.close()
 
 
 def test_step_graph_reports_a_host_check_and_makes_no_graph():

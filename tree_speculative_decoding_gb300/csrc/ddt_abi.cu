@@ -428,8 +428,53 @@ bool is_pinned_host(const void *p) {
     return at.type == cudaMemoryTypeHost;
 }
 
+// Host buffers are pinned host memory, which the GPU reads and writes over the
+// host link through a device pointer (cudaHostGetDevicePointer).  A kernel with
+// one 16-byte load per thread, all in flight at once, moves a step's inputs in a
+// fraction of a copy-engine transfer's latency.  Each thread copies up to four
+// 16-byte units, loads first.
+__device__ unsigned int g_io_edge;  // target of the memset that orders the step after the copy
+__global__ void __launch_bounds__(256) io_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                      size_t n16) {
+    ddt::pdl_trigger();
+    ddt::pdl_wait();  // the output copy may start before the step's last kernel has finished
+    const size_t i0 = (size_t)blockIdx.x * 1024 + threadIdx.x;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (i0 + 256 * k < n16) v[k] = src[i0 + 256 * k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (i0 + 256 * k < n16) dst[i0 + 256 * k] = v[k];
+}
+
+// The device view of a pinned host buffer for a kernel copy of `bytes`, or null
+// when a copy engine transfer must do (no device pointer, 16-byte units only).
+const void *io_device_view(const void *host, const void *dev, size_t bytes) {
+    void *d = nullptr;
+    if (cudaHostGetDevicePointer(&d, const_cast<void *>(host), 0) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if ((reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(dev) | bytes) & 15u) return nullptr;
+    return d;
+}
+
+cudaError_t io_copy(const void *src, void *dst, size_t bytes, cudaStream_t s) {
+    const size_t n16 = bytes / 16;
+    const unsigned ctas = (unsigned)((n16 + 1023) / 1024);
+    return ddt::launch_pdl(io_copy_kernel, dim3(ctas), dim3(256), 0, s, static_cast<const uint4 *>(src),
+                           static_cast<uint4 *>(dst), n16);
+}
+
 // Captures [H2D copy] -> ddt_verify_step -> [D2H copy] on a private stream and
-// instantiates it.
+// instantiates it.  The copies are kernels over the host buffers' device views
+// where possible (else copy-engine transfers).  A 4-byte memset node follows the
+// input copy: the step's first kernel is launched for programmatic dependent
+// launch and reads caller inputs before its wait, and an edge from a non-kernel
+// node is an ordinary one, so the step starts only after the copy is complete.
+// The output copy is launched like the step's kernels and waits on the device for
+// the step's last kernel before it reads anything.
 ddt_status step_graph_create(const ddt_step_args *a, const StepIO &io, ddt_step_graph **graph) {
     if (!a || !graph) return DDT_ERR_INVALID_ARG;
     *graph = nullptr;
@@ -438,15 +483,29 @@ ddt_status step_graph_create(const ddt_step_args *a, const StepIO &io, ddt_step_
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DDT_ERR_CUDA;
     ddt_status st = DDT_ERR_CUDA;
     cudaGraph_t g = nullptr;
+    const void *in_view = io.in_bytes ? io_device_view(io.h_in, io.d_in, io.in_bytes) : nullptr;
+    const void *out_view = io.out_bytes ? io_device_view(io.h_out, io.d_out, io.out_bytes) : nullptr;
+    void *edge = nullptr;
+    if (in_view && cudaGetSymbolAddress(&edge, g_io_edge) != cudaSuccess) {
+        cudaGetLastError();
+        in_view = nullptr;
+    }
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
         st = DDT_OK;
-        if (io.in_bytes &&
-            cudaMemcpyAsync(io.d_in, io.h_in, io.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            st = DDT_ERR_CUDA;
+        if (io.in_bytes) {
+            const bool ok = in_view ? (io_copy(in_view, io.d_in, io.in_bytes, s) == cudaSuccess &&
+                                       cudaMemsetAsync(edge, 0, sizeof(unsigned int), s) == cudaSuccess)
+                                    : cudaMemcpyAsync(io.d_in, io.h_in, io.in_bytes, cudaMemcpyHostToDevice,
+                                                      s) == cudaSuccess;
+            if (!ok) st = DDT_ERR_CUDA;
+        }
         if (st == DDT_OK) st = ddt_verify_step(a, s);
-        if (st == DDT_OK && io.out_bytes &&
-            cudaMemcpyAsync(io.h_out, io.d_out, io.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-            st = DDT_ERR_CUDA;
+        if (st == DDT_OK && io.out_bytes) {
+            const bool ok = out_view ? io_copy(io.d_out, const_cast<void *>(out_view), io.out_bytes, s) == cudaSuccess
+                                     : cudaMemcpyAsync(io.h_out, io.d_out, io.out_bytes, cudaMemcpyDeviceToHost,
+                                                       s) == cudaSuccess;
+            if (!ok) st = DDT_ERR_CUDA;
+        }
         const cudaError_t e = cudaStreamEndCapture(s, &g);  // ends the capture on every path
         if (st == DDT_OK && e != cudaSuccess) st = DDT_ERR_CUDA;
     }
