@@ -187,7 +187,7 @@ def run_device(args, rank, world, local_rank):
     import torch
 
     from tree_speculative_decoding_gb300 import workloads
-    from tree_speculative_decoding_gb300.metrics import attn_flops, kv_bytes
+    from tree_speculative_decoding_gb300.metrics import algorithmic_bytes, attn_flops, kv_bytes
     from tree_speculative_decoding_gb300.pipeline import VerifyStep
 
     dist = None
@@ -368,6 +368,7 @@ def run_device(args, rank, world, local_rank):
         "steps_per_s": round(args.steps * world / elapsed_max, 1),
         "attn_flops_per_step": flops,
         "kv_bytes_per_step": kvb,
+        "algorithmic_bytes_per_step": algorithmic_bytes(wl.kv_indptr, wl.total_q, wl.H, st.total_words),
         "verify_attn_ms": round(attn_mean_ms, 5),
         "l2_flushed": dict(flushed, timing="copy 0's step and ddt_verify_attn graphs, a 256 MiB "
                            "write before each replay (cold code and data), mean"),

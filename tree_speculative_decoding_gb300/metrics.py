@@ -24,3 +24,11 @@ def attn_flops(prefix_len, depth, qo_indptr, H) -> float:
 def kv_bytes(kv_indptr) -> float:
     """Each KV row (576 bf16 = 1152 B) read once per call."""
     return float(kv_indptr[-1]) * D * 2
+
+
+def algorithmic_bytes(kv_indptr, total_q, H, mask_words) -> float:
+    """All bytes one verify-attention call must move at least once: the KV rows,
+    q (576 bf16 per row), the fp32 output (512 per row), the kv indices and the
+    visibility mask words (4 B each)."""
+    rows = float(total_q) * H
+    return kv_bytes(kv_indptr) + rows * D * 2 + rows * DL * 4 + 4.0 * float(kv_indptr[-1]) + 4.0 * mask_words
