@@ -370,6 +370,7 @@ def run_device(args, rank, world, local_rank):
         "kv_bytes_per_step": kvb,
         "algorithmic_bytes_per_step": algorithmic_bytes(wl.kv_indptr, wl.total_q, wl.H, st.total_words),
         "verify_attn_ms": round(attn_mean_ms, 5),
+        "verify_attn_median_ms": round(statistics.median(attn_ms), 5),
         "l2_flushed": dict(flushed, timing="copy 0's step and ddt_verify_attn graphs, a 256 MiB "
                            "write before each replay (cold code and data), mean"),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": tf_burst,
